@@ -1,0 +1,409 @@
+"""Benchmark of the tree speculative-decoding verify step on GB300.
+
+One step = tv_build_ancestors -> tv_tree_attention -> tv_argmax -> tv_tree_walk
+-> tv_commit_kv over one batch of the throughput-stress workload (64 sequences
+x 16384 context tokens, N=32 random trees of depth <= 8, 32 query / 8 KV heads,
+head dim 128, bf16, 16-token blocks behind shuffled block tables, bf16 logits
+over a 151936-token vocabulary).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (fp64, OpenMP over the host cores) on a
+bounded sample of sequences of the same workload, scaled to whole steps.
+Multi-GPU runs (torchrun) are independent replicas: every rank verifies its
+own batch, no collective touches the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("tree-verify steps/s and attention KV GB/s (% of GB300 HBM peak), "
+          "bit-exact walk")
+HBM_FALLBACK_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "tv_tree_attention_stress_traffic.txt")
+ATTN_SOURCES = [os.path.join(ROOT, "tree_speculative_decoding_build_gb300", "csrc", f)
+                for f in ("attention.cu", "attention_tc.cu", "attention.cuh")]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stress")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    for p in ATTN_SOURCES:
+        if os.path.exists(p):
+            with open(p, "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram read+write bytes per launch from the committed ncu summary, or None
+    when it is missing or was taken on a different attention source."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha") != source_digest():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self, timeout=5.0):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
+        self.lines.clear()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in list(self.lines):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def workload_config(inp, name):
+    import numpy as np
+    ctx = inp["ctx_len"].cpu().numpy()
+    return {
+        "workload": (f"{name}: B={inp['B']} ctx={int(ctx.min())}..{int(ctx.max())} N={inp['N']} "
+                     f"Hq/Hkv/D={inp['Hq']}/{inp['Hkv']}/{inp['D']} bf16 KV, block 16, "
+                     f"V={inp['V']} {inp['logits_dtype']} logits"),
+        "batch": inp["B"], "tree_nodes": inp["N"], "ctx_len": int(np.median(ctx)),
+        "window_left": inp["window_left"],
+        "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)",
+    }
+
+
+def attention_algorithmic_bytes(inp):
+    import workloads
+    B, N, Hq, Hkv, D = inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"]
+    kv = workloads.kv_bytes(inp)
+    q = B * N * Hq * D * 2
+    tree_kv = 2 * B * N * Hkv * D * 2
+    out = B * N * Hq * D * 2
+    ctx = inp["ctx_len"].cpu().numpy()
+    table = int(sum((int(c) + 15) // 16 for c in ctx)) * 4
+    return kv + q + tree_kv + out + table
+
+
+def bench_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+    import workloads
+    import tree_speculative_decoding_build_gb300 as tv
+    from tree_speculative_decoding_build_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = workloads.make(args.workload, dev, seed=workloads.get(args.workload).seed + rank)
+    step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
+                         inp["max_blocks"], window_left=inp["window_left"],
+                         logits_dtype=inp["logits_dtype"], device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        step(inp)
+    torch.cuda.synchronize(dev)
+
+    # kernels launched per step: fixed by the launch plan
+    ws_attn = tv.tv_tree_attention_workspace_size(inp["B"], inp["N"], inp["Hq"], inp["Hkv"],
+                                                  inp["D"], inp["max_blocks"], inp["window_left"])
+    dt = tv.TV_F32 if inp["logits_dtype"] == "f32" else tv.TV_BF16
+    ws_arg = tv.tv_argmax_workspace_size(inp["B"] * inp["N"], inp["V"], dt)
+    launches_per_step = 5 + (1 if ws_attn else 0) + (1 if ws_arg else 0)
+
+    # attention timed separately with events around its call, same stream
+    o = step.out
+    B, N = inp["B"], inp["N"]
+
+    def run_step(ev_pair=None):
+        tv.tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], o.anc, o.pos, o.status)
+        if ev_pair is not None:
+            ev_pair[0].record(stream)
+        tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"],
+                             inp["v_cache"], inp["block_table"], inp["ctx_len"], o.pos, o.anc,
+                             o.attn, o.status, window_left=inp["window_left"],
+                             workspace=step.ws_attn)
+        if ev_pair is not None:
+            ev_pair[1].record(stream)
+        tv.tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), step.ws_arg)
+        tv.tv_tree_walk(inp["tokens"], inp["parent"], o.argmax, inp["root_pred"], o.status,
+                        o.out_tokens, o.n_emit, o.acc_nodes, o.n_acc)
+        tv.tv_commit_kv(inp["k_tree"], inp["v_tree"], o.acc_nodes, o.n_acc, inp["ctx_len"],
+                        inp["block_table"], inp["k_cache"], inp["v_cache"], o.ctx_len_out,
+                        o.status)
+
+    K = args.steps
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        run_step(attn_ev[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms = t0.elapsed_time(t1)
+    attn_ms = sum(a.elapsed_time(b) for a, b in attn_ev) / K
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    status_ok = bool((o.status == 0).all().item())
+
+    # end to end through the public API: pinned host inputs in, tokens out
+    host_keys = ["tokens", "parent", "depth", "ctx_len", "root_pred", "block_table", "q",
+                 "k_tree", "v_tree", "logits"]
+    host = {k: inp[k].cpu().pin_memory() for k in host_keys}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res_keys = ["out_tokens", "n_emit", "n_acc", "ctx_len_out"]
+    res_host = {k: torch.empty_like(getattr(o, k), device="cpu").pin_memory() for k in res_keys}
+    d2h = sum(v.numel() * v.element_size() for v in res_host.values())
+    dev_inp = dict(inp)
+    for _ in range(2):
+        for k in host_keys:
+            dev_inp[k].copy_(host[k], non_blocking=True)
+        step(dev_inp)
+        for k in res_keys:
+            res_host[k].copy_(getattr(o, k), non_blocking=True)
+    torch.cuda.synchronize(dev)
+    E = max(1, args.e2e_steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        for k in host_keys:
+            dev_inp[k].copy_(host[k], non_blocking=True)
+        step(dev_inp)
+        for k in res_keys:
+            res_host[k].copy_(getattr(o, k), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / E
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    alg = attention_algorithmic_bytes(inp)
+    achieved = alg / (attn_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": world * K / (ms * 1e-3),
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "impl": "ours",
+        "config": workload_config(inp, args.workload),
+        "attention": {"ms": attn_ms, "kv_gbs": achieved, "algorithmic_bytes": alg,
+                      "frac_of_8tbs_nominal": achieved / 8000.0,
+                      "frac_of_peak": achieved / peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "tv_tree_attention", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(), "peak_source": peak_kind},
+        "e2e": {"value": world / (e2e_ms * 1e-3), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "status_ok": status_ok,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
+    elif not args.no_cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
+    return line
+
+
+def cpu_baseline(name, budget_s=12.0, seqs_max=None):
+    """The oracle, as it stands, on a bounded sample: whole verify steps for a
+    few sequences at a time (all heads, all nodes), until the time budget is
+    spent; scaled to whole-batch steps/s."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    w = workloads.get(name)
+    oracle.build()
+    done, spent = 0, 0.0
+    B = w.B
+    seqs_max = B if seqs_max is None else seqs_max
+    b = 0
+    while done < seqs_max and spent < budget_s:
+        inp = workloads.make(name, "cpu", seed=w.seed + 7919 * (b + 1), B=1)
+        npi = workloads.to_numpy(inp)
+        t = time.perf_counter()
+        oracle.verify_step(npi)
+        spent += time.perf_counter() - t
+        done += 1
+        b += 1
+    per_step = spent / done * B
+    return {"value": 1.0 / per_step, "unit": "steps/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{done} of {B} sequences of the {name} workload, full verify step each "
+                      f"(fp64 attention over all heads/nodes, argmax, walk, commit); "
+                      f"{spent:.1f} s of oracle time scaled by {B}/{done}"}
+
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    K, W = max(1, args.steps), max(0, args.warmup)
+    # each step is a bounded sample: one sequence of the workload, scaled to B
+    import workloads
+    w = workloads.get(args.workload)
+    # keep the whole run within a few minutes
+    K = min(K, 3)
+    W = min(W, 1)
+    for _ in range(W):
+        cpu_baseline(args.workload, budget_s=0.0, seqs_max=1)
+    t = time.perf_counter()
+    vals = [cpu_baseline(args.workload, budget_s=0.0, seqs_max=1) for _ in range(K)]
+    elapsed = time.perf_counter() - t
+    value = sum(v["value"] for v in vals) / len(vals)
+    cb = dict(vals[-1])
+    cb["value"] = value
+    cb["sample"] = (f"each of {K} steps: 1 of {w.B} sequences of the {args.workload} workload, "
+                    f"full verify step, scaled by {w.B}")
+    return {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{args.workload} (oracle on host cores)"},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": elapsed,
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line = bench_ours(args, rank, world, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,374 @@
+"""GPU parity: every step of the CUDA path against the CPU oracle, through the C ABI.
+
+Integer work (masks, positions, argmax, walk, commit) must match bit for bit;
+attention must satisfy |gpu - ref| <= 2e-2 + 1e-2 |ref| against the fp64
+oracle (bf16 inputs, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import assert_close, bf16_to_f64, oracle_attention, step_for, subset_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import tree_speculative_decoding_build_gb300 as m
+    return m
+
+
+def dev_i32(a):
+    return torch.as_tensor(np.ascontiguousarray(a, np.int32), device="cuda")
+
+
+# ------------------------------------------------------------------ ancestors
+
+def test_ancestors_random_and_exhaustive(tv):
+    rng = np.random.Generator(np.random.PCG64(31))
+    cases = []
+    for N in (1, 2, 5, 17, 31, 32, 33, 63, 64):
+        for _ in range(6):
+            cases.append((N, workloads.tree_random(rng, N, 64)))
+    import itertools
+    for p in itertools.product(*[range(-1, t) for t in range(5)]):
+        cases.append((5, np.array(p, np.int32)))
+    by_n = {}
+    for N, par in cases:
+        by_n.setdefault(N, []).append(par)
+    for N, pars in by_n.items():
+        par = np.stack(pars)
+        dep = np.stack([workloads.depths_of(p) for p in pars])
+        ctx = rng.integers(0, 5000, size=len(pars)).astype(np.int32)
+        B = len(pars)
+        anc = torch.empty((B, N), dtype=torch.int64, device="cuda")
+        pos = torch.empty((B, N), dtype=torch.int32, device="cuda")
+        st = torch.full((B,), 77, dtype=torch.int32, device="cuda")
+        tv.tv_build_ancestors(dev_i32(par), dev_i32(dep), dev_i32(ctx), anc, pos, st)
+        mask, opos, ost = oracle.ancestors(par, dep, ctx)
+        bits = anc.cpu().numpy().view(np.uint64)
+        gmask = ((bits[:, :, None] >> np.arange(N, dtype=np.uint64)[None, None, :]) & 1).astype(np.uint8)
+        assert np.array_equal(st.cpu().numpy(), ost)
+        assert np.array_equal(gmask, mask)
+        assert np.array_equal(pos.cpu().numpy(), opos)
+
+
+def test_ancestors_malformed(tv):
+    par = np.stack([workloads.tree_chain(8)] * 4)
+    dep = np.stack([workloads.depths_of(p) for p in par])
+    par[1, 3] = 3
+    par[2, 5] = -7
+    dep[3, 6] = 1
+    anc = torch.empty((4, 8), dtype=torch.int64, device="cuda")
+    pos = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    st = torch.empty((4,), dtype=torch.int32, device="cuda")
+    tv.tv_build_ancestors(dev_i32(par), dev_i32(dep), dev_i32([9] * 4), anc, pos, st)
+    _, _, ost = oracle.ancestors(par, dep, np.full(4, 9))
+    assert list(st.cpu().numpy()) == list(ost) == [0, 2, 2, 2]
+
+
+# ------------------------------------------------------------------ argmax
+
+def bf16_bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("rows,V", [(1, 1), (3, 7), (8, 1024), (16, 262144), (2048, 151936),
+                                    (5, 100003), (300, 4099)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_argmax_matches_oracle(tv, rows, V, dtype):
+    g = torch.Generator(device="cuda").manual_seed(rows * 7 + V)
+    x = torch.randn(rows, V, generator=g, device="cuda")
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    # coarse values and planted ties, also across chunk boundaries
+    if V > 64:
+        x[:, ::97] = 3.5
+        x[0, V // 2] = 9.0
+        x[0, V // 3] = 9.0
+        x[rows - 1, V - 1] = 11.0
+    idx = torch.empty(rows, dtype=torch.int32, device="cuda")
+    tv.tv_argmax(x, idx)
+    ref = oracle.argmax(bf16_bits(x) if dtype == "bf16" else x.cpu().numpy(), dtype)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+def test_argmax_special_values(tv):
+    x = torch.tensor([[-1.0, -0.0, 0.0, -2.0],
+                      [float("nan"), 1.0, 2.0, float("nan")],
+                      [-float("inf")] * 4,
+                      [float("nan")] * 4,
+                      [0.0, -0.0, 0.0, -0.0]], device="cuda")
+    for t, dt in ((x, "f32"), (x.to(torch.bfloat16), "bf16")):
+        idx = torch.empty(5, dtype=torch.int32, device="cuda")
+        tv.tv_argmax(t, idx)
+        assert list(idx.cpu().numpy()) == [1, 2, 0, 0, 0]
+
+
+def test_argmax_strided_and_unaligned_rows(tv):
+    g = torch.Generator(device="cuda").manual_seed(3)
+    base = torch.randn(37, 5003, generator=g, device="cuda").to(torch.bfloat16)
+    x = base[:, :4999]                     # row stride 5003: rows not 16-byte aligned
+    idx = torch.empty(37, dtype=torch.int32, device="cuda")
+    tv.tv_argmax(x, idx)
+    ref = oracle.argmax(bf16_bits(x.contiguous()), "bf16")
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ walk
+
+@pytest.mark.parametrize("family", ["random", "adversarial", "all_wrong", "all_right"])
+def test_walk_matches_oracle_and_greedy(tv, family):
+    rng = np.random.Generator(np.random.PCG64(17))
+    V = 40
+    toks, pars, ams, roots, prefixes, Ns = [], [], [], [], [], []
+    N = 64
+    for b in range(200):
+        n = int(rng.integers(1, N + 1))
+        par = workloads.tree_random(rng, n, 16) if b % 3 else workloads.tree_chain(n)
+        prefix = int(rng.integers(0, 1 << 62))
+        tok, am, rp = workloads.hash_plant(rng, par, V, 0.7, prefix, family)
+        # pad to N with nodes that hang off an unreachable parent token
+        P = np.full(N, -1, np.int32)
+        T = np.full(N, V + 5, np.int32)   # token no prediction can equal
+        A = np.zeros(N, np.int32)
+        P[:n], T[:n], A[:n] = par, tok, am
+        toks.append(T); pars.append(P); ams.append(A); roots.append(rp); prefixes.append(prefix)
+    toks, pars, ams = map(np.stack, (toks, pars, ams))
+    roots = np.array(roots, np.int32)
+    B = len(roots)
+    st = torch.zeros(B, dtype=torch.int32, device="cuda")
+    st[5] = 2                              # a sequence flagged earlier accepts nothing
+    ot = torch.empty((B, N + 1), dtype=torch.int32, device="cuda")
+    ne = torch.empty(B, dtype=torch.int32, device="cuda")
+    an = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    na = torch.empty(B, dtype=torch.int32, device="cuda")
+    tv.tv_tree_walk(dev_i32(toks), dev_i32(pars), dev_i32(ams), dev_i32(roots), st, ot, ne, an, na)
+    r = oracle.walk(toks, pars, ams, roots, st.cpu().numpy())
+    for got, ref in zip((ot, ne, an, na), r):
+        assert np.array_equal(got.cpu().numpy(), ref)
+    ht = workloads.HashTarget(V)
+    ne_h, ot_h = ne.cpu().numpy(), ot.cpu().numpy()
+    for b in range(B):
+        if b == 5:
+            assert ne_h[b] == 1 and ot_h[b, 0] == roots[b]
+            continue
+        assert list(ot_h[b, :ne_h[b]]) == ht.greedy(prefixes[b], int(ne_h[b]))
+
+
+# ------------------------------------------------------------------ commit
+
+def test_commit_matches_oracle_every_length(tv):
+    inp = workloads.make("tiny", "cuda", 12, B=9, ctx=(1, 90), N=16, tree="chain",
+                         shuffle_blocks=True, V=64)
+    B, N = 9, 16
+    n_acc = np.array([min(b * 2, N) for b in range(B)], np.int32)
+    acc = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        acc[b, :n_acc[b]] = np.arange(n_acc[b])
+    npi = workloads.to_numpy(inp)
+    kc = inp["k_cache"].clone()
+    vc = inp["v_cache"].clone()
+    ctx_out = torch.empty(B, dtype=torch.int32, device="cuda")
+    st = torch.zeros(B, dtype=torch.int32, device="cuda")
+    tv.tv_commit_kv(inp["k_tree"], inp["v_tree"], dev_i32(acc), dev_i32(n_acc), inp["ctx_len"],
+                    inp["block_table"], kc, vc, ctx_out, st)
+    rk, rv, rctx, rst = oracle.commit(npi["k_tree"], npi["v_tree"], acc, n_acc, npi["ctx_len"],
+                                      npi["block_table"], npi["k_cache"], npi["v_cache"])
+    assert np.array_equal(bf16_bits(kc), rk) and np.array_equal(bf16_bits(vc), rv)
+    assert np.array_equal(ctx_out.cpu().numpy(), rctx)
+    assert np.array_equal(st.cpu().numpy(), rst)
+
+
+def test_commit_bad_blocks(tv):
+    inp = workloads.make("tiny", "cuda", 4, B=3, ctx=(31, 31), N=4, tree="chain", V=64)
+    npi = workloads.to_numpy(inp)
+    bt = npi["block_table"].copy()
+    bt[1, 2] = npi["k_cache"].shape[0]
+    bt[2, 2:] = -1
+    acc = np.tile(np.arange(4, dtype=np.int32), (3, 1))
+    n_acc = np.full(3, 4, np.int32)
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    ctx_out = torch.empty(3, dtype=torch.int32, device="cuda")
+    st = torch.zeros(3, dtype=torch.int32, device="cuda")
+    tv.tv_commit_kv(inp["k_tree"], inp["v_tree"], dev_i32(acc), dev_i32(n_acc), inp["ctx_len"],
+                    dev_i32(bt), kc, vc, ctx_out, st)
+    rk, rv, rctx, rst = oracle.commit(npi["k_tree"], npi["v_tree"], acc, n_acc, npi["ctx_len"],
+                                      bt, npi["k_cache"], npi["v_cache"])
+    assert list(st.cpu().numpy()) == list(rst) == [0, 3, 3]
+    assert np.array_equal(bf16_bits(kc), rk) and np.array_equal(ctx_out.cpu().numpy(), rctx)
+
+
+# ------------------------------------------------------------------ attention
+
+def run_attention(tv, inp, num_splits=0, window_left=None):
+    B, N = inp["B"], inp["N"]
+    wl = inp["window_left"] if window_left is None else window_left
+    anc = torch.empty((B, N), dtype=torch.int64, device="cuda")
+    pos = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(inp["q"])
+    tv.tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], anc, pos, st)
+    tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
+                         inp["block_table"], inp["ctx_len"], pos, anc, out, st, window_left=wl,
+                         num_splits=num_splits)
+    torch.cuda.synchronize()
+    return out, st
+
+
+SMALL = [
+    # (workload, overrides)
+    ("tiny", dict()),
+    ("tiny", dict(B=3, ctx=(0, 50), N=8, tree="random")),
+    ("tiny", dict(B=2, ctx=(1, 17), N=1, tree="star")),
+    ("leaf_sibling", dict(ctx=333)),
+    ("best_first", dict(B=2, ctx=(100, 700), V=1000)),
+    ("best_first", dict(B=2, ctx=(100, 700), N=64, tree="random", V=1000)),
+    ("window", dict(B=2, ctx=(600, 1500), V=1000)),
+    ("window", dict(B=2, ctx=(20, 90), window_left=3, V=1000)),
+    ("window", dict(B=2, ctx=(20, 90), window_left=0, V=1000)),
+    ("stress", dict(B=3, ctx=(0, 300), V=1000)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_attention_small_full_check(tv, case, splits):
+    name, kw = SMALL[case]
+    inp = workloads.make(name, "cuda", 100 + case, **kw)
+    out, st = run_attention(tv, inp, num_splits=splits)
+    assert (st.cpu().numpy() == 0).all()
+    npi = workloads.to_numpy(inp)
+    ref = oracle_attention(npi)
+    assert_close(bf16_to_f64(out), ref, f"{name} {kw} splits={splits}")
+
+
+def test_attention_bitwise_deterministic_and_block_order_free(tv):
+    inp = workloads.make("best_first", "cuda", 7, B=4, ctx=(300, 900), V=1000, shuffle_blocks=True)
+    a, _ = run_attention(tv, inp)
+    b, _ = run_attention(tv, inp)
+    assert torch.equal(a, b)
+    # same physical content under another block numbering -> identical bits
+    perm = torch.randperm(inp["num_blocks"], generator=torch.Generator().manual_seed(1)).cuda()
+    inv = torch.argsort(perm).to(torch.int32)
+    inp2 = dict(inp)
+    inp2["k_cache"] = inp["k_cache"][perm]
+    inp2["v_cache"] = inp["v_cache"][perm]
+    bt = inp["block_table"]
+    inp2["block_table"] = torch.where(bt >= 0, inv[bt.clamp(min=0).long()], bt)
+    c, _ = run_attention(tv, inp2)
+    assert torch.equal(a, c)
+
+
+def test_attention_bad_block_sets_status(tv):
+    inp = workloads.make("tiny", "cuda", 3, B=2, ctx=(40, 40), N=4, tree="chain", V=64)
+    inp["block_table"] = inp["block_table"].clone()
+    inp["block_table"][1, 1] = 10 ** 6
+    out, st = run_attention(tv, inp)
+    assert list(st.cpu().numpy()) == [0, 3]
+    assert torch.isfinite(out.float()).all()
+
+
+FULL = ["tiny", "leaf_sibling", "best_first", "window", "stress"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_attention_full_size_sampled(tv, name):
+    """Each workload at its full size, in the launch configuration the benchmark
+    times; the oracle checks a sample of sequences and heads."""
+    inp = workloads.make(name, "cuda", V=1000)   # logits are irrelevant here
+    out, st = run_attention(tv, inp)
+    assert (st.cpu().numpy() == 0).all()
+    B = inp["B"]
+    seqs = sorted({0, B - 1, B // 2})
+    heads = sorted({0, inp["Hq"] - 1, inp["Hq"] // 2 + 1}) if inp["Hq"] > 2 else None
+    npi = subset_numpy(inp, seqs)
+    ref = oracle_attention(npi, head_sel=heads)
+    got = bf16_to_f64(out[torch.as_tensor(seqs, device="cuda")])
+    if heads is not None:
+        got, ref = got[:, :, heads], ref[:, :, heads]
+    assert_close(got, ref, name)
+    if name == "window":
+        out_g, _ = run_attention(tv, inp, window_left=-1)
+        npi["window_left"] = -1
+        ref_g = oracle_attention(npi, head_sel=heads)
+        got_g = bf16_to_f64(out_g[torch.as_tensor(seqs, device="cuda")])
+        if heads is not None:
+            got_g, ref_g = got_g[:, :, heads], ref_g[:, :, heads]
+        assert_close(got_g, ref_g, "window/global")
+
+
+# ------------------------------------------------------------------ whole step
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", dict()),
+    ("tiny", dict(plant="hash")),
+    ("leaf_sibling", dict(ctx=500)),
+    ("best_first", dict(B=4, ctx=(200, 900))),
+    ("stress", dict(B=4, ctx=(50, 400), plant="path")),
+    ("stress", dict(B=4, ctx=(50, 400), plant="hash:adversarial")),
+])
+def test_whole_step_matches_oracle(tv, name, kw):
+    inp = workloads.make(name, "cuda", 55, **kw)
+    npi = workloads.to_numpy(inp)
+    step = step_for(inp)
+    o = step(inp)
+    torch.cuda.synchronize()
+    ref = oracle.verify_step(npi)
+    bits = o.anc.cpu().numpy().view(np.uint64)
+    N = inp["N"]
+    gmask = ((bits[:, :, None] >> np.arange(N, dtype=np.uint64)[None, None, :]) & 1).astype(np.uint8)
+    assert np.array_equal(gmask, ref["mask"])
+    assert np.array_equal(o.pos.cpu().numpy(), ref["pos"])
+    assert np.array_equal(o.status.cpu().numpy(), ref["status"])
+    assert_close(bf16_to_f64(o.attn), ref["attn"], name)
+    for k in ("argmax", "out_tokens", "n_emit", "acc_nodes", "n_acc", "ctx_len_out"):
+        assert np.array_equal(getattr(o, k).cpu().numpy(), ref[k]), k
+    assert np.array_equal(bf16_bits(inp["k_cache"]), ref["k_cache"])
+    assert np.array_equal(bf16_bits(inp["v_cache"]), ref["v_cache"])
+    if kw.get("plant") == "path":
+        assert (o.n_acc.cpu().numpy() >= 1).all()
+
+
+def test_whole_step_full_size_stress(tv):
+    """The benchmark's workload (64 x 16384 context, shuffled blocks) with one
+    planted root-to-leaf path per sequence: integer outputs checked in full,
+    attention and cache sampled / checked by property."""
+    inp = workloads.make("stress", "cuda", plant="path")
+    kc0 = inp["k_cache"].clone()
+    step = step_for(inp)
+    o = step(inp)
+    torch.cuda.synchronize()
+    st = o.status.cpu().numpy()
+    assert (st == 0).all()
+    # integer path in full: argmax over all 2048 rows, then walk
+    B, N = inp["B"], inp["N"]
+    logits = inp["logits"].view(B * N, -1)
+    am_ref = oracle.argmax(bf16_bits(logits), "bf16").reshape(B, N)
+    assert np.array_equal(o.argmax.cpu().numpy(), am_ref)
+    npi_small = {k: inp[k].cpu().numpy() for k in ("tokens", "parent", "root_pred")}
+    r = oracle.walk(npi_small["tokens"], npi_small["parent"], am_ref, npi_small["root_pred"], st)
+    for got, ref in zip((o.out_tokens, o.n_emit, o.acc_nodes, o.n_acc), r):
+        assert np.array_equal(got.cpu().numpy(), ref)
+    assert (o.n_acc.cpu().numpy() >= 1).all()
+    # commit: the accepted rows sit at positions ctx .. ctx+n_acc-1, nothing else moved
+    n_acc = o.n_acc.cpu().numpy()
+    acc = o.acc_nodes.cpu().numpy()
+    ctx = inp["ctx_len"].cpu().numpy()
+    bt = inp["block_table"].cpu().numpy()
+    touched = torch.zeros(inp["num_blocks"], 16, dtype=torch.bool, device="cuda")
+    for b in range(B):
+        for i in range(n_acc[b]):
+            p = ctx[b] + i
+            blk = bt[b, p // 16]
+            touched[blk, p % 16] = True
+            assert torch.equal(inp["k_cache"][blk, :, p % 16], inp["k_tree"][b, acc[b, i]])
+            assert torch.equal(inp["v_cache"][blk, :, p % 16], inp["v_tree"][b, acc[b, i]])
+    keep = ~touched
+    assert torch.equal(inp["k_cache"].transpose(1, 2)[keep], kc0.transpose(1, 2)[keep])
+    assert np.array_equal(o.ctx_len_out.cpu().numpy(), ctx + n_acc)

@@ -1,0 +1,83 @@
+"""Tree speculative-decoding verify step on GB300 (sm_103a).
+
+The step is five calls of the C library ``libtv.so`` (see ``include/tv.h``),
+bound here through ctypes with the same names:
+
+    tv_build_ancestors -> tv_tree_attention -> tv_argmax -> tv_tree_walk -> tv_commit_kv
+
+``VerifyStep`` owns the output and scratch buffers of one batch shape and
+enqueues the five calls on one CUDA stream with no host synchronisation.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from ._lib import (  # noqa: F401
+    BLOCK_SIZE, EXPORTS, LIB_PATH, TV_BF16, TV_ERR_ARG, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_TREE,
+    TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError, status_string, tv_argmax,
+    tv_argmax_workspace_size, tv_build_ancestors, tv_commit_kv, tv_tree_attention,
+    tv_tree_attention_workspace_size, tv_tree_walk)
+
+
+@dataclasses.dataclass
+class StepOutputs:
+    anc: torch.Tensor          # int64 [B, N] ancestor-or-self bitmask
+    pos: torch.Tensor          # int32 [B, N] position ids
+    status: torch.Tensor       # int32 [B]
+    attn: torch.Tensor         # bf16 [B, N, Hq, D]
+    argmax: torch.Tensor       # int32 [B, N]
+    out_tokens: torch.Tensor   # int32 [B, N+1]
+    n_emit: torch.Tensor       # int32 [B]
+    acc_nodes: torch.Tensor    # int32 [B, N]
+    n_acc: torch.Tensor        # int32 [B]
+    ctx_len_out: torch.Tensor  # int32 [B]
+
+
+class VerifyStep:
+    """One verify step for a fixed batch shape; buffers are allocated once."""
+
+    def __init__(self, B, N, Hq, Hkv, D, V, max_blocks, window_left=-1, logits_dtype="bf16",
+                 num_splits=0, device="cuda"):
+        dev = torch.device(device)
+        i32 = torch.int32
+        self.shape = dict(B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, V=V, max_blocks=max_blocks)
+        self.window_left = window_left
+        self.num_splits = num_splits
+        self.out = StepOutputs(
+            anc=torch.empty((B, N), dtype=torch.int64, device=dev),
+            pos=torch.empty((B, N), dtype=i32, device=dev),
+            status=torch.empty((B,), dtype=i32, device=dev),
+            attn=torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev),
+            argmax=torch.empty((B, N), dtype=i32, device=dev),
+            out_tokens=torch.empty((B, N + 1), dtype=i32, device=dev),
+            n_emit=torch.empty((B,), dtype=i32, device=dev),
+            acc_nodes=torch.empty((B, N), dtype=i32, device=dev),
+            n_acc=torch.empty((B,), dtype=i32, device=dev),
+            ctx_len_out=torch.empty((B,), dtype=i32, device=dev),
+        )
+        ws_attn = tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left,
+                                                   num_splits)
+        dt = TV_F32 if logits_dtype == "f32" else TV_BF16
+        ws_arg = tv_argmax_workspace_size(B * N, V, dt)
+        self.ws_attn = torch.empty(max(ws_attn, 1), dtype=torch.uint8, device=dev)
+        self.ws_arg = torch.empty(max(ws_arg, 1), dtype=torch.uint8, device=dev)
+
+    def __call__(self, inp, stream=None) -> StepOutputs:
+        """Enqueue the whole step for ``inp`` (dict of device tensors)."""
+        o = self.out
+        B, N = inp["tokens"].shape
+        tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], o.anc, o.pos, o.status,
+                           stream)
+        tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
+                          inp["block_table"], inp["ctx_len"], o.pos, o.anc, o.attn, o.status,
+                          window_left=self.window_left, num_splits=self.num_splits,
+                          workspace=self.ws_attn, stream=stream)
+        tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), self.ws_arg, stream)
+        tv_tree_walk(inp["tokens"], inp["parent"], o.argmax, inp["root_pred"], o.status,
+                     o.out_tokens, o.n_emit, o.acc_nodes, o.n_acc, stream)
+        tv_commit_kv(inp["k_tree"], inp["v_tree"], o.acc_nodes, o.n_acc, inp["ctx_len"],
+                     inp["block_table"], inp["k_cache"], inp["v_cache"], o.ctx_len_out, o.status,
+                     stream)
+        return o

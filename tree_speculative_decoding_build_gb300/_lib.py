@@ -1,0 +1,224 @@
+"""ctypes binding of libtv.so: argument marshalling only.
+
+Each ``tv_*`` function here has the name and argument order of the C entry
+point in ``include/tv.h``; it checks dtypes, devices and contiguity of the
+torch tensors it is given, passes their device pointers, and raises
+``TvError`` on a non-zero host status.  All arithmetic runs in the library's
+CUDA kernels; there is no fallback of any kind: without the compiled library
+importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = _build.LIB
+
+TV_OK, TV_ERR_ARG, TV_ERR_TREE, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_UNSUPPORTED = range(6)
+TV_F32, TV_BF16 = 0, 1
+BLOCK_SIZE = 16
+
+EXPORTS = (
+    "tv_status_string",
+    "tv_build_ancestors",
+    "tv_tree_attention_workspace_size",
+    "tv_tree_attention",
+    "tv_argmax_workspace_size",
+    "tv_argmax",
+    "tv_tree_walk",
+    "tv_commit_kv",
+)
+
+
+class TvError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        super().__init__(f"{fn}: {status_string(code)} (status {code})")
+
+
+class AttnArgs(ctypes.Structure):
+    """Mirror of ``tv_attn_args``."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("ctx_len", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+        ("anc", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int),
+        ("num_blocks", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
+        ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int),
+        ("out", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libtv.so is not built ({LIB_PATH}); run "
+            "`python -c 'import __graft_entry__ as g; g.build()'` first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, L, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.tv_status_string.argtypes = [I]
+    lib.tv_status_string.restype = ctypes.c_char_p
+    lib.tv_build_ancestors.argtypes = [P, P, P, I, I, P, P, P, P]
+    lib.tv_tree_attention_workspace_size.argtypes = [ctypes.POINTER(AttnArgs)]
+    lib.tv_tree_attention_workspace_size.restype = S
+    lib.tv_tree_attention.argtypes = [ctypes.POINTER(AttnArgs), P, S, P]
+    lib.tv_argmax_workspace_size.argtypes = [L, L, I]
+    lib.tv_argmax_workspace_size.restype = S
+    lib.tv_argmax.argtypes = [P, I, L, L, L, P, P, S, P]
+    lib.tv_tree_walk.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]
+    lib.tv_commit_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
+    for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
+              "tv_commit_kv"):
+        getattr(lib, f).restype = I
+    return lib
+
+
+lib = _load()
+
+
+def status_string(code: int) -> str:
+    return lib.tv_status_string(int(code)).decode()
+
+
+def _check(fn, code):
+    if code != TV_OK:
+        raise TvError(fn, code)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def tv_build_ancestors(parent, depth, ctx_len, anc, pos, status, stream=None):
+    B, N = parent.shape
+    _check("tv_build_ancestors", lib.tv_build_ancestors(
+        _ptr(parent, torch.int32, "parent"), _ptr(depth, torch.int32, "depth"),
+        _ptr(ctx_len, torch.int32, "ctx_len"), B, N, _ptr(anc, torch.int64, "anc"),
+        _ptr(pos, torch.int32, "pos"), _ptr(status, torch.int32, "status"), _stream(stream)))
+
+
+def attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
+              window_left=-1, window_right=0, sm_scale=0.0, num_splits=0):
+    bf = torch.bfloat16
+    B, N, Hq, D = q.shape
+    a = AttnArgs()
+    a.q = _ptr(q, bf, "q")
+    a.k_tree = _ptr(k_tree, bf, "k_tree")
+    a.v_tree = _ptr(v_tree, bf, "v_tree")
+    a.k_cache = _ptr(k_cache, bf, "k_cache")
+    a.v_cache = _ptr(v_cache, bf, "v_cache")
+    a.block_table = _ptr(block_table, torch.int32, "block_table")
+    a.ctx_len = _ptr(ctx_len, torch.int32, "ctx_len")
+    a.pos = _ptr(pos, torch.int32, "pos")
+    a.anc = _ptr(anc, torch.int64, "anc")
+    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, k_tree.shape[2], D
+    a.block_size = k_cache.shape[2]
+    a.max_blocks = block_table.shape[1]
+    a.num_blocks = k_cache.shape[0]
+    a.window_left = int(window_left)
+    a.window_right = int(window_right)
+    a.sm_scale = float(sm_scale)
+    a.num_splits = int(num_splits)
+    a.out = _ptr(out, bf, "out")
+    a.status = _ptr(status, torch.int32, "status")
+    return a
+
+
+def tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left=-1, num_splits=0):
+    a = AttnArgs()
+    a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, Hkv, D
+    a.block_size = BLOCK_SIZE
+    a.max_blocks = max_blocks
+    a.window_left = window_left
+    a.window_right = 0
+    a.num_splits = num_splits
+    return int(lib.tv_tree_attention_workspace_size(ctypes.byref(a)))
+
+
+def tv_tree_attention(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out,
+                      status, window_left=-1, window_right=0, sm_scale=0.0, num_splits=0,
+                      workspace=None, stream=None):
+    a = attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
+                  window_left, window_right, sm_scale, num_splits)
+    need = int(lib.tv_tree_attention_workspace_size(ctypes.byref(a)))
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wp = _ptr(workspace, None, "workspace") if workspace is not None else None
+    wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tv_tree_attention", lib.tv_tree_attention(ctypes.byref(a), wp, wb, _stream(stream)))
+
+
+def tv_argmax_workspace_size(rows, V, dtype):
+    return int(lib.tv_argmax_workspace_size(rows, V, dtype))
+
+
+def _logits_dtype(t):
+    if t.dtype == torch.bfloat16:
+        return TV_BF16
+    if t.dtype == torch.float32:
+        return TV_F32
+    raise TypeError(f"logits: unsupported dtype {t.dtype}")
+
+
+def tv_argmax(logits, out_idx, workspace=None, stream=None):
+    """Row argmax of a 2-D ``logits`` [rows, V] (rows may be strided)."""
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits: expected a 2-D tensor with unit inner stride")
+    if not logits.is_cuda:
+        raise ValueError("logits: must be a CUDA tensor")
+    rows, V = logits.shape
+    dt = _logits_dtype(logits)
+    need = tv_argmax_workspace_size(rows, V, dt)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    wp = _ptr(workspace, None, "workspace") if workspace is not None else None
+    wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tv_argmax", lib.tv_argmax(ctypes.c_void_p(logits.data_ptr()), dt, rows, V,
+                                      logits.stride(0), _ptr(out_idx, torch.int32, "out_idx"),
+                                      wp, wb, _stream(stream)))
+
+
+def tv_tree_walk(tokens, parent, argmax, root_pred, status, out_tokens, n_emit, acc_nodes, n_acc,
+                 stream=None):
+    B, N = tokens.shape
+    i32 = torch.int32
+    _check("tv_tree_walk", lib.tv_tree_walk(
+        _ptr(tokens, i32, "tokens"), _ptr(parent, i32, "parent"), _ptr(argmax, i32, "argmax"),
+        _ptr(root_pred, i32, "root_pred"), _ptr(status, i32, "status"), B, N,
+        _ptr(out_tokens, i32, "out_tokens"), _ptr(n_emit, i32, "n_emit"),
+        _ptr(acc_nodes, i32, "acc_nodes"), _ptr(n_acc, i32, "n_acc"), _stream(stream)))
+
+
+def tv_commit_kv(k_tree, v_tree, acc_nodes, n_acc, ctx_len_in, block_table, k_cache, v_cache,
+                 ctx_len_out, status, stream=None):
+    B, N, Hkv, D = k_tree.shape
+    i32, bf = torch.int32, torch.bfloat16
+    _check("tv_commit_kv", lib.tv_commit_kv(
+        _ptr(k_tree, bf, "k_tree"), _ptr(v_tree, bf, "v_tree"), _ptr(acc_nodes, i32, "acc_nodes"),
+        _ptr(n_acc, i32, "n_acc"), _ptr(ctx_len_in, i32, "ctx_len_in"),
+        _ptr(block_table, i32, "block_table"), B, N, Hkv, D, block_table.shape[1],
+        k_cache.shape[0], _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
+        _ptr(ctx_len_out, i32, "ctx_len_out"), _ptr(status, i32, "status"), _stream(stream)))
