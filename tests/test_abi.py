@@ -13,8 +13,8 @@ HEADER = os.path.join(ROOT, "include", "tv.h")
 
 @pytest.fixture(scope="module")
 def lib():
-    from tree_speculative_decoding_build_gb300 import build
-    path = build.build()
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
     return ctypes.CDLL(path)
 
 
