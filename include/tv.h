@@ -53,6 +53,7 @@ typedef int tv_status;
 #define TV_ERR_BLOCK 3        /* block id or block-table slot out of range        */
 #define TV_ERR_CUDA 4         /* a CUDA launch or driver call failed              */
 #define TV_ERR_UNSUPPORTED 5  /* valid but not supported shape or dtype           */
+#define TV_ERR_SCRATCH_LIMIT 6 /* too large for a no-allocation entry point's fixed scratch */
 
 #define TV_F32 0
 #define TV_BF16 1
@@ -178,6 +179,33 @@ size_t tv_argmax_workspace_size(int64_t rows, int64_t V, int dtype);
 tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
                     int64_t row_stride, int32_t *out_idx, void *workspace,
                     size_t workspace_bytes, tv_stream stream);
+
+/*
+ * tv_argmax_noalloc -- tv_argmax for callers that cannot allocate device memory.
+ * The verify-step pages have no counterpart to this call; it exists for the
+ * library's users.  Some callers may not call cudaMalloc at all while they
+ * run: a serving loop whose device memory is all owned by one pool allocator,
+ * a plugin host that hands a kernel only its input and output buffers, or a
+ * latency-critical decode loop in which cudaMalloc (which can synchronise the
+ * device) is not allowed.  Such callers cannot provide tv_argmax's workspace.
+ *
+ * Same arguments, result and errors as tv_argmax, minus the workspace.  The
+ * split partials live in one fixed array of 8192 (value, index) pairs (64 KiB)
+ * in the library's static device memory, which every GPU that loads the
+ * library keeps until the process exits.  A shape whose plan needs more pairs
+ * than that returns TV_ERR_SCRATCH_LIMIT and launches nothing (on a 152-SM GPU
+ * no shape needs more than about 2,500).  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call made with a given device current looks up the array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.  Every call shares the one array and leaves its partials
+ * behind (each call writes every partial it reads, so nothing needs clearing),
+ * so calls that may overlap on the GPU -- on different streams without
+ * ordering between them -- race and must not be issued.
+ */
+tv_status tv_argmax_noalloc(const void *logits, int dtype, int64_t rows, int64_t V,
+                            int64_t row_stride, int32_t *out_idx, tv_stream stream);
 
 /*
  * tv_tree_walk -- greedy acceptance walk over the tree, on the GPU.

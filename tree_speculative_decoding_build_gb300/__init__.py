@@ -15,9 +15,9 @@ import dataclasses
 import torch
 
 from ._lib import (  # noqa: F401
-    BLOCK_SIZE, EXPORTS, LIB_PATH, TV_BF16, TV_ERR_ARG, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_TREE,
-    TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError, status_string, tv_argmax,
-    tv_argmax_workspace_size, tv_build_ancestors, tv_commit_kv, tv_tree_attention,
+    BLOCK_SIZE, EXPORTS, LIB_PATH, TV_BF16, TV_ERR_ARG, TV_ERR_BLOCK, TV_ERR_CUDA,
+    TV_ERR_SCRATCH_LIMIT, TV_ERR_TREE, TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError, status_string,
+    tv_argmax, tv_argmax_noalloc, tv_argmax_workspace_size, tv_build_ancestors, tv_commit_kv, tv_tree_attention,
     tv_tree_attention_workspace_size, tv_tree_walk)
 
 

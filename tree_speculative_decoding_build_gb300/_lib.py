@@ -19,7 +19,8 @@ from . import build as _build
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = _build.LIB
 
-TV_OK, TV_ERR_ARG, TV_ERR_TREE, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_UNSUPPORTED = range(6)
+(TV_OK, TV_ERR_ARG, TV_ERR_TREE, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_UNSUPPORTED,
+ TV_ERR_SCRATCH_LIMIT) = range(7)
 TV_F32, TV_BF16 = 0, 1
 BLOCK_SIZE = 16
 
@@ -30,6 +31,7 @@ EXPORTS = (
     "tv_tree_attention",
     "tv_argmax_workspace_size",
     "tv_argmax",
+    "tv_argmax_noalloc",
     "tv_tree_walk",
     "tv_commit_kv",
 )
@@ -72,6 +74,8 @@ def _load():
     lib.tv_argmax_workspace_size.argtypes = [L, L, I]
     lib.tv_argmax_workspace_size.restype = S
     lib.tv_argmax.argtypes = [P, I, L, L, L, P, P, S, P]
+    lib.tv_argmax_noalloc.argtypes = [P, I, L, L, L, P, P]
+    lib.tv_argmax_noalloc.restype = I
     lib.tv_tree_walk.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]
     lib.tv_commit_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
@@ -199,6 +203,20 @@ def tv_argmax(logits, out_idx, workspace=None, stream=None):
     _check("tv_argmax", lib.tv_argmax(ctypes.c_void_p(logits.data_ptr()), dt, rows, V,
                                       logits.stride(0), _ptr(out_idx, torch.int32, "out_idx"),
                                       wp, wb, _stream(stream)))
+
+
+def tv_argmax_noalloc(logits, out_idx, stream=None):
+    """``tv_argmax`` without a workspace: for callers that may not allocate
+    device memory (see include/tv.h).  Calls that could overlap on the GPU
+    share one scratch array and must not be issued."""
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits: expected a 2-D tensor with unit inner stride")
+    if not logits.is_cuda:
+        raise ValueError("logits: must be a CUDA tensor")
+    rows, V = logits.shape
+    _check("tv_argmax_noalloc", lib.tv_argmax_noalloc(
+        ctypes.c_void_p(logits.data_ptr()), _logits_dtype(logits), rows, V, logits.stride(0),
+        _ptr(out_idx, torch.int32, "out_idx"), _stream(stream)))
 
 
 def tv_tree_walk(tokens, parent, argmax, root_pred, status, out_tokens, n_emit, acc_nodes, n_acc,

@@ -15,6 +15,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <vector>
+
 #include "common.cuh"
 
 namespace tv {
@@ -214,6 +217,79 @@ extern "C" tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int6
     pv = static_cast<float *>(workspace);
     pi = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
                                      ((n * sizeof(float) + 255) / 256) * 256);
+  }
+  const bool vec = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) &&
+                   ((row_stride * esize) % 16 == 0);
+  const unsigned grid = (unsigned)(rows * p.chunks);
+  cudaStream_t s = as_stream(stream);
+  if (dtype == TV_BF16)
+    argmax_chunk_kernel<__nv_bfloat16><<<grid, kArgThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(logits), (int)V, row_stride, p.chunks, p.chunk_len, vec,
+        pv, pi, out_idx);
+  else
+    argmax_chunk_kernel<float><<<grid, kArgThreads, 0, s>>>(
+        static_cast<const float *>(logits), (int)V, row_stride, p.chunks, p.chunk_len, vec, pv, pi,
+        out_idx);
+  if (p.chunks > 1) {
+    const int wpb = 8;
+    argmax_final_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, s>>>(pv, pi, rows,
+                                                                              p.chunks, out_idx);
+  }
+  return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// tv_argmax_noalloc: the same argmax for callers that cannot allocate device
+// memory.  Its split partials live in a fixed file-scope device array instead
+// of a caller-provided workspace.
+//
+// Device code could name the array directly; host code must not pass its name
+// to a kernel (on the host the name is only a stand-in, not a device address),
+// so the address is fetched once per device with cudaGetSymbolAddress and
+// cached.
+namespace tv {
+namespace {
+
+constexpr size_t kNoAllocPairs = 8192;  // (value, index) partials: 64 KiB in all
+static __device__ __align__(256) unsigned char g_argmax_scratch[kNoAllocPairs * 8];
+
+// Device address of g_argmax_scratch on the current device (set up on the
+// first call made with that device current), or nullptr on failure.
+void *noalloc_scratch() {
+  static std::mutex mu;
+  static std::vector<void *> addr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if ((int)addr.size() <= dev) addr.resize(dev + 1, nullptr);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_argmax_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace tv
+
+extern "C" tv_status tv_argmax_noalloc(const void *logits, int dtype, int64_t rows, int64_t V,
+                                       int64_t row_stride, int32_t *out_idx, tv_stream stream) {
+  if (dtype != TV_F32 && dtype != TV_BF16) return TV_ERR_UNSUPPORTED;
+  if (rows < 0 || V < 1 || row_stride < V || V > INT32_MAX - 1024) return TV_ERR_ARG;
+  if (rows == 0) return TV_OK;
+  if (rows > (int64_t)INT32_MAX) return TV_ERR_ARG;
+  if (!logits || !out_idx) return TV_ERR_ARG;
+  const int esize = dtype == TV_F32 ? 4 : 2;
+  const ArgmaxPlan p = plan_argmax(rows, V, esize);
+  float *pv = nullptr;
+  int32_t *pi = nullptr;
+  if (p.chunks > 1) {
+    if ((unsigned long long)rows * p.chunks > kNoAllocPairs) return TV_ERR_SCRATCH_LIMIT;
+    char *base = static_cast<char *>(noalloc_scratch());
+    if (!base) return TV_ERR_CUDA;
+    pv = reinterpret_cast<float *>(base);
+    pi = reinterpret_cast<int32_t *>(base + kNoAllocPairs * sizeof(float));
   }
   const bool vec = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) &&
                    ((row_stride * esize) % 16 == 0);

@@ -187,6 +187,7 @@ extern "C" const char *tv_status_string(tv_status s) {
     case TV_ERR_BLOCK: return "block id or block-table slot out of range";
     case TV_ERR_CUDA: return "CUDA error";
     case TV_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case TV_ERR_SCRATCH_LIMIT: return "size exceeds the fixed scratch of a no-allocation entry point";
     default: return "unknown status";
   }
 }
