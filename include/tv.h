@@ -109,12 +109,20 @@ tv_status tv_build_ancestors(const int32_t *parent, const int32_t *depth,
  *   window_right must be -1 or >= 0; every visible key precedes or equals the
  *                query position, so the right bound never removes a key
  *   sm_scale   softmax scale on q.k; 0 means 1/sqrt(D)
- *   num_splits context splits per (sequence, KV head); 0 = chosen by the library
+ *   num_splits context splits per (sequence, KV head) of the CUDA-core kernel;
+ *              0 = chosen by the library (the tensor-core kernel balances its
+ *              work itself and ignores it)
+ *   kernel     0 = automatic (tensor cores when the shape allows, else CUDA
+ *              cores), 1 = CUDA-core kernel, 2 = tensor-core kernel
+ *              (TV_ERR_UNSUPPORTED outside its shapes: D = 128,
+ *              (Hq/Hkv)*N <= 128, B <= 1024)
  *   out        bf16 [B, N, Hq, D]         softmax(scale q.K^T) V per node and head
  *   status     int32 [B]                  TV_ERR_BLOCK is recorded when a needed
  *                                         block id is outside [0, num_blocks) or
- *                                         ctx_len exceeds max_blocks*16 (the
- *                                         offending keys are skipped)
+ *                                         ctx_len exceeds max_blocks*16 (that
+ *                                         sequence's outputs are then
+ *                                         unspecified but finite); TV_ERR_CUDA
+ *                                         when a pipeline wait timed out
  * Query head h reads KV head h / (Hq / Hkv).  Supported: D in {64, 128, 256},
  * Hq % Hkv == 0, block_size == 16, N <= 64, (Hq/Hkv)*N <= 256.
  */
@@ -136,6 +144,7 @@ typedef struct tv_attn_args {
   int window_right;
   float sm_scale;
   int num_splits;
+  int kernel;
   void *out;
   int32_t *status;
 } tv_attn_args;

@@ -206,7 +206,7 @@ def test_commit_bad_blocks(tv):
 
 # ------------------------------------------------------------------ attention
 
-def run_attention(tv, inp, num_splits=0, window_left=None):
+def run_attention(tv, inp, num_splits=0, window_left=None, kernel=0):
     B, N = inp["B"], inp["N"]
     wl = inp["window_left"] if window_left is None else window_left
     anc = torch.empty((B, N), dtype=torch.int64, device="cuda")
@@ -216,7 +216,7 @@ def run_attention(tv, inp, num_splits=0, window_left=None):
     tv.tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], anc, pos, st)
     tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
                          inp["block_table"], inp["ctx_len"], pos, anc, out, st, window_left=wl,
-                         num_splits=num_splits)
+                         num_splits=num_splits, kernel=kernel)
     torch.cuda.synchronize()
     return out, st
 
@@ -233,25 +233,45 @@ SMALL = [
     ("window", dict(B=2, ctx=(20, 90), window_left=3, V=1000)),
     ("window", dict(B=2, ctx=(20, 90), window_left=0, V=1000)),
     ("stress", dict(B=3, ctx=(0, 300), V=1000)),
+    ("best_first", dict(B=3, ctx=(1, 200), N=16, tree="random", V=1000)),     # R = 64 rows
+    ("best_first", dict(B=2, ctx=(5, 90), N=7, tree="random", V=1000)),       # node tile padded
+    ("window", dict(B=5, ctx=(0, 70), N=1, tree="star", window_left=17, V=1000)),
+    ("stress", dict(B=40, ctx=(1, 40), V=1000)),   # more (sequence, head) pairs than SMs
 ]
+
+# (kernel, num_splits): automatic choice (tensor cores for head dim 128), then
+# the CUDA-core kernel with one and with three context splits
+MODES = [(0, 0), (1, 1), (1, 3), (2, 0)]
 
 
 @pytest.mark.parametrize("case", range(len(SMALL)))
-@pytest.mark.parametrize("splits", [0, 1, 3])
-def test_attention_small_full_check(tv, case, splits):
+@pytest.mark.parametrize("mode", range(len(MODES)))
+def test_attention_small_full_check(tv, case, mode):
     name, kw = SMALL[case]
+    kernel, splits = MODES[mode]
+    w = workloads.get(name)
+    if kernel == 2 and (w.D != 128 or (w.Hq // w.Hkv) * kw.get("N", w.N) > 128):
+        pytest.skip("the tensor-core kernel covers head dim 128 and <= 128 rows per KV head")
     inp = workloads.make(name, "cuda", 100 + case, **kw)
-    out, st = run_attention(tv, inp, num_splits=splits)
+    out, st = run_attention(tv, inp, num_splits=splits, kernel=kernel)
     assert (st.cpu().numpy() == 0).all()
     npi = workloads.to_numpy(inp)
     ref = oracle_attention(npi)
-    assert_close(bf16_to_f64(out), ref, f"{name} {kw} splits={splits}")
+    assert_close(bf16_to_f64(out), ref, f"{name} {kw} kernel={kernel} splits={splits}")
 
 
-def test_attention_bitwise_deterministic_and_block_order_free(tv):
+def test_tensor_core_kernel_rejects_other_shapes(tv):
+    inp = workloads.make("tiny", "cuda", 1, V=64)           # head dim 64
+    with pytest.raises(tv.TvError) as e:
+        run_attention(tv, inp, kernel=2)
+    assert e.value.code == tv.TV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_attention_bitwise_deterministic_and_block_order_free(tv, kernel):
     inp = workloads.make("best_first", "cuda", 7, B=4, ctx=(300, 900), V=1000, shuffle_blocks=True)
-    a, _ = run_attention(tv, inp)
-    b, _ = run_attention(tv, inp)
+    a, _ = run_attention(tv, inp, kernel=kernel)
+    b, _ = run_attention(tv, inp, kernel=kernel)
     assert torch.equal(a, b)
     # same physical content under another block numbering -> identical bits
     perm = torch.randperm(inp["num_blocks"], generator=torch.Generator().manual_seed(1)).cuda()
@@ -261,7 +281,7 @@ def test_attention_bitwise_deterministic_and_block_order_free(tv):
     inp2["v_cache"] = inp["v_cache"][perm]
     bt = inp["block_table"]
     inp2["block_table"] = torch.where(bt >= 0, inv[bt.clamp(min=0).long()], bt)
-    c, _ = run_attention(tv, inp2)
+    c, _ = run_attention(tv, inp2, kernel=kernel)
     assert torch.equal(a, c)
 
 

@@ -53,7 +53,7 @@ class AttnArgs(ctypes.Structure):
         ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
         ("D", ctypes.c_int), ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int),
         ("num_blocks", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
-        ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int),
+        ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("kernel", ctypes.c_int),
         ("out", ctypes.c_void_p), ("status", ctypes.c_void_p),
     ]
 
@@ -124,8 +124,11 @@ def tv_build_ancestors(parent, depth, ctx_len, anc, pos, status, stream=None):
         _ptr(pos, torch.int32, "pos"), _ptr(status, torch.int32, "status"), _stream(stream)))
 
 
+KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TENSOR_CORE = 0, 1, 2
+
+
 def attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
-              window_left=-1, window_right=0, sm_scale=0.0, num_splits=0):
+              window_left=-1, window_right=0, sm_scale=0.0, num_splits=0, kernel=0):
     bf = torch.bfloat16
     B, N, Hq, D = q.shape
     a = AttnArgs()
@@ -146,13 +149,16 @@ def attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, an
     a.window_right = int(window_right)
     a.sm_scale = float(sm_scale)
     a.num_splits = int(num_splits)
+    a.kernel = int(kernel)
     a.out = _ptr(out, bf, "out")
     a.status = _ptr(status, torch.int32, "status")
     return a
 
 
-def tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left=-1, num_splits=0):
+def tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left=-1, num_splits=0,
+                                     kernel=0):
     a = AttnArgs()
+    a.kernel = kernel
     a.B, a.N, a.Hq, a.Hkv, a.D = B, N, Hq, Hkv, D
     a.block_size = BLOCK_SIZE
     a.max_blocks = max_blocks
@@ -164,9 +170,9 @@ def tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left=-
 
 def tv_tree_attention(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out,
                       status, window_left=-1, window_right=0, sm_scale=0.0, num_splits=0,
-                      workspace=None, stream=None):
+                      workspace=None, stream=None, kernel=0):
     a = attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
-                  window_left, window_right, sm_scale, num_splits)
+                  window_left, window_right, sm_scale, num_splits, kernel)
     need = int(lib.tv_tree_attention_workspace_size(ctypes.byref(a)))
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)

@@ -355,14 +355,22 @@ using namespace tv;
 
 namespace {
 
-// Which kernel serves these arguments: 1 = tcgen05, 0 = CUDA cores.
-bool use_tc(const tv_attn_args *a) {
+// Which kernel serves these arguments: true = tcgen05, false = CUDA cores.
+// kernel 2 (tensor cores) on a shape the tcgen05 kernel does not cover is
+// reported by the caller as TV_ERR_UNSUPPORTED.
+bool tc_shape(const tv_attn_args *a) {
   AttnParams probe{};
+  probe.B = a->B;
   probe.D = a->D;
   probe.G = a->Hkv > 0 ? a->Hq / a->Hkv : 0;
   probe.N = a->N;
   probe.R = probe.G * a->N;
   return attention_tc_supported(probe);
+}
+
+bool use_tc(const tv_attn_args *a) {
+  if (a->kernel == 1) return false;
+  return tc_shape(a);
 }
 
 size_t workspace_bytes_for(const tv_attn_args *a, int splits) {
@@ -376,8 +384,9 @@ size_t workspace_bytes_for(const tv_attn_args *a, int splits) {
 
 extern "C" size_t tv_tree_attention_workspace_size(const tv_attn_args *a) {
   if (!a || !shape_ok(a) || a->Hq % a->Hkv != 0) return 0;
+  if (use_tc(a)) return attention_tc_workspace(a->B, sm_count());
   const int R = (a->Hq / a->Hkv) * a->N;
-  const SplitPlan sp = plan_splits(a, R, use_tc(a));
+  const SplitPlan sp = plan_splits(a, R, false);
   return workspace_bytes_for(a, sp.splits);
 }
 
@@ -387,6 +396,8 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   if (a->block_size != kBlock) return TV_ERR_UNSUPPORTED;
   if (a->D != 64 && a->D != 128 && a->D != 256) return TV_ERR_UNSUPPORTED;
   if (a->Hq % a->Hkv != 0) return TV_ERR_ARG;
+  if (a->kernel < 0 || a->kernel > 2) return TV_ERR_ARG;
+  if (a->kernel == 2 && !tc_shape(a)) return TV_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const int R = G * a->N;
   if (R > 256) return TV_ERR_UNSUPPORTED;
@@ -402,7 +413,7 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   if (align & 15) return TV_ERR_ARG;
   const bool tc = use_tc(a);
   const SplitPlan sp = plan_splits(a, R, tc);
-  const size_t need = workspace_bytes_for(a, sp.splits);
+  const size_t need = tc ? attention_tc_workspace(a->B, sm_count()) : workspace_bytes_for(a, sp.splits);
   if (need > workspace_bytes || (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))))
     return TV_ERR_ARG;
 
@@ -430,7 +441,7 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   p.qscale = scale * 1.4426950408889634f;
   p.splits = sp.splits;
   p.bps = sp.bps;
-  if (sp.splits > 1) {
+  if (!tc && sp.splits > 1) {
     const size_t rows = (size_t)a->B * a->Hkv * sp.splits * R;
     p.part_o = static_cast<float *>(workspace);
     p.part_ml = reinterpret_cast<float2 *>(static_cast<char *>(workspace) +
@@ -440,10 +451,10 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   p.status = a->status;
   cudaStream_t s = as_stream(stream);
   if (tc) {
-    if (launch_attention_tc(p, s) != cudaSuccess) return TV_ERR_CUDA;
-  } else {
-    launch_attention_generic(p, s);
+    if (launch_attention_tc(p, workspace, s) != cudaSuccess) return TV_ERR_CUDA;
+    return TV_OK;
   }
+  launch_attention_generic(p, s);
   if (sp.splits > 1) launch_combine(p, s);
   return launch_status();
 }

@@ -52,9 +52,11 @@ void launch_combine(const AttnParams &p, cudaStream_t stream);
 // CUDA-core kernel: any supported D and row count.
 void launch_attention_generic(const AttnParams &p, cudaStream_t stream);
 
-// Tensor-core (tcgen05) kernel for D = 128 and R <= 128.  Returns false when
-// the shape is not covered, so the caller falls back to the generic kernel.
+// Tensor-core (tcgen05) kernel for D = 128 and R <= 128 rows per KV head.
 bool attention_tc_supported(const AttnParams &p);
-cudaError_t launch_attention_tc(const AttnParams &p, cudaStream_t stream);
+// Scratch of the tensor-core kernel: schedule offsets and split partials.
+size_t attention_tc_workspace(int B, int num_ctas);
+// Launches the kernel (one CTA per SM) and its partial combine.
+cudaError_t launch_attention_tc(const AttnParams &p, void *workspace, cudaStream_t stream);
 
 }  // namespace tv
