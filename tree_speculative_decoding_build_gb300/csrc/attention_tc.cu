@@ -19,7 +19,7 @@
 //              O += P_j V_j (V read as an MN-major operand) into TMEM O.
 //   warps 2-5  softmax: thread r owns row r; reads S_j from TMEM, applies the
 //              context / window / ancestor mask, keeps the running max and sum,
-//              writes P_j (bf16) to swizzled shared memory.  O is rescaled in
+//              writes P_j (bf16 pairs) to TMEM, where the P V product reads it.  O is rescaled in
 //              TMEM only when the row max grows by more than 2^8 (the final
 //              division by the running sum makes any reference max exact).
 // Work balance: the (sequence, KV head, tile) list, ragged in sequence length,
@@ -47,21 +47,25 @@ using namespace ptx;
 constexpr int kD = 128;
 constexpr int kM = 128;                 // UMMA M: rows per tile
 constexpr int kBN = 64;                 // keys per context tile (4 paged blocks)
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
+constexpr int kStages = 5;
+constexpr int kWarps = 11;               // producer, S issuer, 2 softmax warpgroups, producer
+constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxB = 1024;             // sequences the in-CTA schedule can hold
 constexpr uint32_t kQChunk = kM * 64 * 2;              // [128 rows][64 d] bf16 = 16 KB
 constexpr uint32_t kKVChunk = kBN * 64 * 2;            // [64 keys][64 d] bf16 = 8 KB
-constexpr uint32_t kStageBytes = 4 * kKVChunk;         // K (2 chunks) + V (2 chunks)
-constexpr uint32_t kPBytes = kM * kBN * 2;             // [128 rows][64 keys] bf16 = 16 KB
+constexpr uint32_t kStageBytes = 4 * kKVChunk;         // K (16 KB) + V (16 KB)
+constexpr uint32_t kHalfStage = 2 * kKVChunk;          // V starts here within a stage
+constexpr uint32_t kBlkChunk = kBlock * 64 * 2;        // [16 keys][64 d] bf16 = 2 KB
+constexpr uint32_t kBlkBytes = 2 * kBlkChunk;          // one paged block: [2 halves][16][64]
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffKV = 2 * kQChunk;
-constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffPre = kOffP + 2 * kPBytes;
+constexpr uint32_t kOffPre = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffCtx = kOffPre + 4 * (kMaxB + 1);
-constexpr uint32_t kSmemBytes = kOffCtx + 4 * kMaxB + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 256;     // S0 [0,64), S1 [64,128), O [128,256)
+constexpr uint32_t kOffMerge = (kOffCtx + 4 * kMaxB + 15) / 16 * 16;   // [2][128] float2
+constexpr uint32_t kSmemBytes = kOffMerge + 2 * kM * 8 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 512;     // S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448)
 constexpr uint32_t kColO = 128;
+constexpr uint32_t kColP = 384;         // P as bf16 pairs: 64 keys = 32 columns
 constexpr float kTau = 8.0f;            // rescale O only when the max grows by > 2^8
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait at most
 
@@ -80,10 +84,13 @@ struct Bars {
   unsigned long long kv_empty[kStages];
   unsigned long long q_full, q_empty;
   unsigned long long s_full[2];
+  unsigned long long s_free[2];
   unsigned long long p_full[2];
   unsigned long long pv_done[2];
+  unsigned long long merge;
   unsigned long long o_free;
   unsigned long long fin;
+  unsigned long long fin_pv[2];
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -107,6 +114,10 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile in
       }
     }
   }
+}
+
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  return mbar_try_wait(bar, parity) || wait_bar(bar, parity, abort_flag);
 }
 
 // UMMA shared-memory descriptor, 128-byte swizzle (sm_100 layout):
@@ -246,11 +257,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(smem_u32(&bars.q_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
+      mbar_init(smem_u32(&bars.s_free[i]), 128);
       mbar_init(smem_u32(&bars.p_full[i]), 128);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
+    mbar_init(smem_u32(&bars.merge), 128);
     mbar_init(smem_u32(&bars.o_free), 128);
     mbar_init(smem_u32(&bars.fin), 1);
+    mbar_init(smem_u32(&bars.fin_pv[0]), 1);
+    mbar_init(smem_u32(&bars.fin_pv[1]), 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -268,60 +283,149 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
   Cursor cur{s_pre, B, Hkv, hi, hi, 0, 0, 0, 1};
   if (lo < hi) cur.locate(lo);  // an empty range leaves f == hi: nothing to do
 
-  if (warp == 0) {
-    // ======================================================== TMA producer
-    if (lane == 0) {
+  if (warp == 0 || warp == kWarps - 1) {
+    // ======================================================== TMA producers
+    // Two warps share the tiles: warp 0 loads even tiles and every Q tile, the
+    // last warp loads odd tiles.  Each runs the whole loop (block ids are
+    // fetched 32 slots at a time, one per lane, one window ahead) and skips
+    // the tiles of the other.
+    const int par = warp == 0 ? 0 : 1;
+    if (lane == 0 && par == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_kc);
       prefetch_tensormap(&tm_vc);
       prefetch_tensormap(&tm_kt);
       prefetch_tensormap(&tm_vt);
     }
-    long long j = 0;
+    int j = 0;
     int seg = 0;
-    int ctx = 0, blk_lo = 0;
+    int q_pending = -1, q_b = 0, q_kvh = 0;  // segment whose Q copy is not issued yet
+    int ctx = 0, blk_lo = 0, nblk_end = 0, nfull = 0;
+    int win_base = 0, cur_id = -1, nxt_id = -1;
     bool ok = true;
+    auto load_id = [&](int b, int slot) -> int {
+      return slot < nblk_end ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
+    };
+    auto issue_q = [&]() {
+      if (lane == 0) {
+        const uint32_t qb = smem_u32(&bars.q_full);
+        mbar_arrive_expect_tx(qb, 2u * R * 128u);
+        tma_load_3d(sbase + kOffQ, &tm_q, qb, 0, q_kvh * G, q_b * N);
+        tma_load_3d(sbase + kOffQ + kQChunk, &tm_q, qb, 64, q_kvh * G, q_b * N);
+      }
+      q_pending = -1;
+    };
     while (ok && cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
       if (cur.seg_start(lo)) {
-        if (lane == 0 && seg > 0) ok = wait_bar(smem_u32(&bars.q_empty), (seg - 1) & 1, abort_flag);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (lane == 0) {
-          const uint32_t qb = smem_u32(&bars.q_full);
-          mbar_arrive_expect_tx(qb, 2u * R * 128u);
-          tma_load_3d(sbase + kOffQ, &tm_q, qb, 0, kvh * G, b * N);
-          tma_load_3d(sbase + kOffQ + kQChunk, &tm_q, qb, 64, kvh * G, b * N);
+        if (q_pending >= 0) {  // the previous segment's Q is still waiting: finish it first
+          if (lane == 0 && q_pending > 0)
+            ok = wait_fast(smem_u32(&bars.q_empty), (q_pending - 1) & 1, abort_flag);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          issue_q();
         }
         ctx = s_ctx[b];
         blk_lo = first_visible_block(ctx, p.window_left);
+        nblk_end = (ctx + kBlock - 1) / kBlock;
+        nfull = ctx / kBlock;
+        win_base = blk_lo + 4 * cur.u;  // a CTA's range may start mid-pair
+        cur_id = load_id(b, win_base + lane);
+        nxt_id = load_id(b, win_base + 32 + lane);
+        if (par == 0) {
+          q_pending = seg;
+          q_b = b;
+          q_kvh = kvh;
+        }
         ++seg;
       }
-      const int stage = (int)(j % kStages);
-      if (lane == 0 && j >= kStages)
-        ok = wait_bar(smem_u32(&bars.kv_empty[stage]), (uint32_t)((j / kStages - 1) & 1), abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      const int nct = cur.tiles - 1;
+      const int slot0 = blk_lo + 4 * cur.u;
+      if (cur.u < nct && slot0 - win_base >= 32) {
+        win_base += 32;
+        cur_id = nxt_id;
+        nxt_id = load_id(b, win_base + 32 + lane);
+      }
+      if ((j & 1) != par) {  // the other producer's tile
+        ++j;
+        cur.next();
+        continue;
+      }
+      const int stage = j % kStages;
+      const uint32_t empty_parity = (uint32_t)((j / kStages - 1) & 1);
+      if (q_pending < 0) {
+        // common case: every lane waits for the stage itself (no broadcasts)
+        if (j >= kStages) {
+          ok = __all_sync(0xffffffffu,
+                          wait_fast(smem_u32(&bars.kv_empty[stage]), empty_parity, abort_flag));
+          if (!ok) break;
+        }
+      } else {
+        // acquire the stage, issuing the pending Q copy as soon as Q is free
+        bool got = j < kStages;
+        uint64_t t0 = 0;
+        for (uint32_t spin = 0;; ++spin) {
+          int qr = 0, gr = got;
+          if (lane == 0) {
+            if (q_pending >= 0)
+              qr = q_pending == 0 || mbar_test_wait(smem_u32(&bars.q_empty), (q_pending - 1) & 1);
+            if (!gr) gr = mbar_test_wait(smem_u32(&bars.kv_empty[stage]), empty_parity);
+          }
+          qr = __shfl_sync(0xffffffffu, qr, 0);
+          gr = __shfl_sync(0xffffffffu, gr, 0);
+          if (qr) issue_q();
+          got = gr;
+          if (got) break;
+          if ((spin & 63) == 63) {
+            int bad = 0;
+            if (lane == 0) {
+              const uint64_t now = globaltimer();
+              if (t0 == 0) t0 = now;
+              if (*abort_flag || now - t0 > kWaitNs) {
+                *abort_flag = 1;
+                bad = 1;
+              }
+            }
+            if (__shfl_sync(0xffffffffu, bad, 0)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (!ok) break;
+      }
       unsigned char *st = smem + kOffKV + stage * kStageBytes;
       const uint32_t st_addr = sbase + kOffKV + stage * kStageBytes;
       const uint32_t fb = smem_u32(&bars.kv_full[stage]);
-      const int nct = cur.tiles - 1;
       if (cur.u < nct) {
         // context tile: paged blocks blk_lo + 4u .. +3
+        // fast path: four whole blocks with valid ids.  Lane c < 8 copies K of
+        // block c/2 (d half c%2) into [half][64 keys][64], lanes 8-11 copy V of
+        // block c-8 whole ([half][16][64]); every lane works out its own copy.
+        const int fblk = lane < 8 ? (lane >> 1) : ((lane - 8) & 3);
+        const int fid = __shfl_sync(0xffffffffu, cur_id, (slot0 - win_base + fblk) & 31);
+        const bool fgood = lane >= 12 || (fid >= 0 && fid < p.num_blocks);
+        if (__all_sync(0xffffffffu, fgood) && slot0 + 4 <= nfull) {
+          if (lane == 0) mbar_arrive_expect_tx(fb, kStageBytes);
+          __syncwarp();
+          const int row0 = (fid * Hkv + kvh) * kBlock;
+          if (lane < 8)
+            tma_load_2d(st_addr + (lane & 1) * kKVChunk + fblk * kBlkChunk, &tm_kc, fb, 64 * (lane & 1),
+                        row0);
+          else if (lane < 12)
+            tma_load_3d(st_addr + kHalfStage + fblk * kBlkBytes, &tm_vc, fb, 0, row0, 0);
+        } else {
         int ids[4], rows[4];
         uint32_t bytes = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int slot = blk_lo + 4 * cur.u + i;
+          const int slot = slot0 + i;
           int r = ctx - slot * kBlock;
           r = r < 0 ? 0 : (r > kBlock ? kBlock : r);
-          int id = -1;
-          if (r > 0) {
-            id = p.block_table[(size_t)b * p.max_blocks + slot];
-            if (id < 0 || id >= p.num_blocks) {
-              if (lane == 0) set_status(p.status, b, TV_ERR_BLOCK);
-              r = 0;
-            }
+          int id = __shfl_sync(0xffffffffu, cur_id, slot - win_base);
+          if (r > 0 && (id < 0 || id >= p.num_blocks)) {
+            if (lane == 0) set_status(p.status, b, TV_ERR_BLOCK);
+            r = 0;
           }
           ids[i] = id;
           rows[i] = r;
@@ -333,135 +437,122 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int i = 0; i < 4; ++i) {
           if (rows[i] == kBlock) continue;
           zeroed = true;
-          const int nz = (kBlock - rows[i]) * 8;  // 16-byte words per chunk
+          const int nz = (kBlock - rows[i]) * 8;  // 16-byte words per half
           for (int w = lane; w < 4 * nz; w += 32) {
-            const int c = w / nz, k = w - c * nz;
-            *reinterpret_cast<uint4 *>(st + c * kKVChunk + (i * kBlock + rows[i]) * 128 + k * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int kc = w / nz, k = w - kc * nz;  // kc: 0,1 = K halves, 2,3 = V halves
+            const int r = rows[i] * 128 + k * 16;
+            const uint32_t off = kc < 2 ? kc * kKVChunk + i * kBlkChunk + r
+                                        : kHalfStage + i * kBlkBytes + (kc - 2) * kBlkChunk + r;
+            *reinterpret_cast<uint4 *>(st + off) = make_uint4(0, 0, 0, 0);
           }
         }
         if (zeroed) fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, bytes);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (rows[i] == 0) continue;
+        // whole blocks: lanes 0-7 copy K (block lane/2, d half lane%2) into the
+        // [half][64 keys][64] K tile, lanes 8-11 copy V block lane-8 whole
+        // ([half][16][64]); copies issued by several lanes go out together
+        if (lane < 12) {
+          const int i = lane < 8 ? lane >> 1 : lane - 8;
+          if (rows[i] == kBlock) {
             const int row0 = (ids[i] * Hkv + kvh) * kBlock;
-            const uint32_t dk = st_addr + i * kBlock * 128;
-            const uint32_t dv = dk + 2 * kKVChunk;
-            if (rows[i] == kBlock) {
-              tma_load_2d(dk, &tm_kc, fb, 0, row0);
-              tma_load_2d(dk + kKVChunk, &tm_kc, fb, 64, row0);
-              tma_load_2d(dv, &tm_vc, fb, 0, row0);
-              tma_load_2d(dv + kKVChunk, &tm_vc, fb, 64, row0);
+            if (lane < 8) {
+              const int h = lane & 1;
+              tma_load_2d(st_addr + h * kKVChunk + i * kBlkChunk, &tm_kc, fb, 64 * h, row0);
             } else {
-              for (int r = 0; r < rows[i]; ++r) {
-                tma_load_2d(dk + r * 128, &tm_kc_row, fb, 0, row0 + r);
-                tma_load_2d(dk + kKVChunk + r * 128, &tm_kc_row, fb, 64, row0 + r);
-                tma_load_2d(dv + r * 128, &tm_vc_row, fb, 0, row0 + r);
-                tma_load_2d(dv + kKVChunk + r * 128, &tm_vc_row, fb, 64, row0 + r);
-              }
+              tma_load_3d(st_addr + kHalfStage + i * kBlkBytes, &tm_vc, fb, 0, row0, 0);
             }
           }
         }
-      } else {
-        // node tile: rows 0..N-1 from k_tree / v_tree, rows N..NP-1 zero
-        if (NP > N) {
-          const int nz = (NP - N) * 8;
-          for (int w = lane; w < 4 * nz; w += 32) {
-            const int c = w / nz, k = w - c * nz;
-            *reinterpret_cast<uint4 *>(st + c * kKVChunk + N * 128 + k * 16) = make_uint4(0, 0, 0, 0);
+        // a partial last block: row by row
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (rows[i] == 0 || rows[i] == kBlock) continue;
+            const int row0 = (ids[i] * Hkv + kvh) * kBlock;
+            const uint32_t dk = st_addr + i * kBlkChunk, dv = st_addr + kHalfStage + i * kBlkBytes;
+            for (int r = 0; r < rows[i]; ++r) {
+              tma_load_2d(dk + r * 128, &tm_kc_row, fb, 0, row0 + r);
+              tma_load_2d(dk + kKVChunk + r * 128, &tm_kc_row, fb, 64, row0 + r);
+              tma_load_2d(dv + r * 128, &tm_vc_row, fb, 0, row0 + r);
+              tma_load_2d(dv + kBlkChunk + r * 128, &tm_vc_row, fb, 64, row0 + r);
+            }
           }
-          fence_proxy_async_smem();
+        }
+        }
+      } else {
+        // node tile: K rows 0..NP-1 per d half (3-D copy of all nodes of the
+        // head), V per 16-node group ([half][16][64]); rows past N hold the
+        // next sequence's nodes (finite, masked) or zero fill past the end
+        if (lane == 0) {
+          const int groups = NP / 16;
+          mbar_arrive_expect_tx(fb, 2u * groups * kBlkBytes);
+          for (int gi = 0; gi < groups; ++gi) {
+            tma_load_3d(st_addr + gi * kBlkChunk, &tm_kt, fb, 0, kvh, b * N + 16 * gi);
+            tma_load_3d(st_addr + kKVChunk + gi * kBlkChunk, &tm_kt, fb, 64, kvh, b * N + 16 * gi);
+            tma_load_4d(st_addr + kHalfStage + gi * kBlkBytes, &tm_vt, fb, 0, kvh, b * N + 16 * gi, 0);
+          }
         }
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(fb, 4u * N * 128u);
-          tma_load_3d(st_addr, &tm_kt, fb, 0, kvh, b * N);
-          tma_load_3d(st_addr + kKVChunk, &tm_kt, fb, 64, kvh, b * N);
-          tma_load_3d(st_addr + 2 * kKVChunk, &tm_vt, fb, 0, kvh, b * N);
-          tma_load_3d(st_addr + 3 * kKVChunk, &tm_vt, fb, 64, kvh, b * N);
-        }
       }
       ++j;
       cur.next();
     }
+    if (ok && q_pending >= 0) {  // the last segment's Q: the MMA is waiting for it
+      if (lane == 0 && q_pending > 0)
+        ok = wait_fast(smem_u32(&bars.q_empty), (q_pending - 1) & 1, abort_flag);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) issue_q();
+    }
     if (!ok && lane == 0) {
       // give copies still in flight a bounded chance to land before exit
       int dummy = 0;
-      for (long long k = j > kStages ? j - kStages : 0; k < j; ++k)
-        wait_bar(smem_u32(&bars.kv_full[k % kStages]), (uint32_t)((k / kStages) & 1), &dummy);
-      if (seg > 0) wait_bar(smem_u32(&bars.q_full), (seg - 1) & 1, &dummy);
+      for (int k = j > kStages ? j - kStages : 0; k < j; ++k)
+        if ((k & 1) == par) wait_bar(smem_u32(&bars.kv_full[k % kStages]), (uint32_t)((k / kStages) & 1), &dummy);
+      if (par == 0 && seg > 0) wait_bar(smem_u32(&bars.q_full), (seg - 1) & 1, &dummy);
       set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
     }
   } else if (warp == 1) {
-    // ======================================================== MMA issuer
+    // ======================================================== S issuer
+    // One thread issues S_j = Q K_j^T for every tile in order: it needs the
+    // K tile, Q of the segment, and the S buffer (j&1) read out by the softmax
+    // (s_free of tile j-2, signalled right after the softmax loaded S, so S of
+    // the next tile is computed while the softmax still works on the current
+    // one).  The P V products are issued by the softmax warpgroups themselves.
     if (lane == 0) {
-      const uint32_t idesc_pv = make_idesc(kM, kD, true);
+      const uint64_t dq = sw128_desc(sbase + kOffQ, 16, 1024);
+      const uint64_t dk = sw128_desc(sbase + kOffKV, 16, 1024);
       bool ok = true;
-      long long j = 0;
+      int js = 0;
       int seg = 0;
-      // pending PV (tile j-1): stage, node-tile flag, first-in-segment, segment ordinal
-      int pv_stage = 0, pv_keys = 0, pv_first = 0, pv_seg = 0;
-      bool pv_pending = false;
-      auto issue_pv = [&](long long jj) -> bool {
-        if (!wait_bar(smem_u32(&bars.p_full[jj & 1]), (uint32_t)((jj >> 1) & 1), abort_flag))
-          return false;
-        if (pv_first && pv_seg > 0)
-          if (!wait_bar(smem_u32(&bars.o_free), (uint32_t)((pv_seg - 1) & 1), abort_flag))
-            return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + kOffP + (uint32_t)(jj & 1) * kPBytes;
-        const uint32_t va = sbase + kOffKV + pv_stage * kStageBytes + 2 * kKVChunk;
-        for (int ks = 0; ks < pv_keys / 16; ++ks) {
-          const uint64_t ad = sw128_desc(pa + ks * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(va + ks * 2048, kKVChunk, 1024);
-          umma_f16(tmem + kColO, ad, bd, idesc_pv, (ks > 0 || !pv_first) ? 1u : 0u);
-        }
-        umma_commit(smem_u32(&bars.pv_done[jj & 1]));
-        umma_commit(smem_u32(&bars.kv_empty[pv_stage]));
-        return true;
-      };
       while (ok && cur.valid()) {
         const bool first = cur.seg_start(lo);
-        const bool last = cur.seg_end();
-        if (first) {
-          ok = wait_bar(smem_u32(&bars.q_full), seg & 1, abort_flag);
-          if (!ok) break;
-          ++seg;
-        }
-        const int stage = (int)(j % kStages);
-        ok = wait_bar(smem_u32(&bars.kv_full[stage]), (uint32_t)((j / kStages) & 1), abort_flag);
+        const int stage = js % kStages;
+        if (js >= 2)
+          ok = wait_fast(smem_u32(&bars.s_free[js & 1]), (uint32_t)(((js - 2) >> 1) & 1), abort_flag);
+        if (ok && first) ok = wait_fast(smem_u32(&bars.q_full), (uint32_t)(seg & 1), abort_flag);
+        if (ok) ok = wait_fast(smem_u32(&bars.kv_full[stage]), (uint32_t)((js / kStages) & 1), abort_flag);
         if (!ok) break;
         tc_fence_after();
-        const bool node = cur.u == cur.tiles - 1;
-        const int keys = node ? NP : kBN;
+        if (first) ++seg;
+        const bool last = cur.seg_end();
+        const int keys = cur.u == cur.tiles - 1 ? NP : kBN;
         const uint32_t idesc_s = make_idesc(kM, keys, false);
-        const uint32_t ka = sbase + kOffKV + stage * kStageBytes;
-        const uint32_t sc = tmem + (uint32_t)(j & 1) * kBN;
+        // start-address field = address >> 4: byte offsets are added as offset >> 4
+        const uint64_t bk = dk + (uint64_t)((stage * kStageBytes) >> 4);
+        const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
+        // Q and K are [2 d halves][rows][64], 128-byte swizzled
 #pragma unroll
         for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t c = ks >> 2, kk = ks & 3;
-          const uint64_t ad = sw128_desc(sbase + kOffQ + c * kQChunk + kk * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(ka + c * kKVChunk + kk * 32, 16, 1024);
-          umma_f16(sc, ad, bd, idesc_s, ks > 0 ? 1u : 0u);
+          const uint32_t off_q = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
+          const uint32_t off_k = ((ks >> 2) * kKVChunk + (ks & 3) * 32) >> 4;
+          umma_f16(sc, dq + off_q, bk + off_k, idesc_s, ks > 0 ? 1u : 0u);
         }
-        umma_commit(smem_u32(&bars.s_full[j & 1]));
+        umma_commit(smem_u32(&bars.s_full[js & 1]));
         if (last) umma_commit(smem_u32(&bars.q_empty));
-        if (pv_pending) {
-          ok = issue_pv(j - 1);
-          if (!ok) break;
-        }
-        pv_pending = true;
-        pv_stage = stage;
-        pv_keys = keys;
-        pv_first = first;
-        pv_seg = seg - 1;
-        ++j;
+        ++js;
         cur.next();
       }
-      if (ok && pv_pending) ok = issue_pv(j - 1);
       // every MMA issued so far has completed once this arrives
       umma_commit(smem_u32(&bars.fin));
       int dummy = 0;
@@ -470,15 +561,22 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
   } else {
     // ======================================================== softmax / epilogue
+    // Two warpgroups take alternate tiles (x = parity of the CTA-wide tile
+    // counter), each with its own running max / sum and its own O accumulator
+    // in TMEM; at the end of a (sequence, KV head) segment warpgroup 0 merges
+    // the two.  Thread (warp, lane) owns row 32*(warp%4) + lane == its TMEM lane.
+    const int x = (warp - 2) >> 2;                    // warpgroup 0 or 1
     const int quad = warp & 3;
-    const int m = quad * 32 + lane;                   // row == TMEM lane
+    const int m = quad * 32 + lane;
     const uint32_t tlane = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t t_s = tlane + (uint32_t)x * kBN;
+    const uint32_t t_o = tlane + kColO + (uint32_t)x * kD;
     const bool row_ok = m < R;
     const int t = row_ok ? m / G : 0;
     const int g = row_ok ? m - t * G : 0;
     const float qscale = p.qscale;
     const int wl = p.window_left;
-    long long j = 0;
+    long long j = 0, last_j = -1;
     int seg = 0;
     bool ok = true;
     float m_used = -INFINITY, l = 0.f;
@@ -486,13 +584,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     unsigned long long allowed = 0;
     long long seg_f0 = lo;
     bool seg_complete = false;
-    const uint32_t p_row = (uint32_t)m * 128u;
-    const uint32_t sw = (uint32_t)(m & 7);
+    const uint32_t t_p = tlane + kColP + (uint32_t)x * 32;
+    const uint32_t idesc_pv = make_idesc(kM, kD, true);
+    const uint64_t dv0 = sw128_desc(sbase + kOffKV + kHalfStage, kBlkChunk, 1024);
     while (cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
       if (cur.seg_start(lo)) {
         m_used = -INFINITY;
         l = 0.f;
+        last_j = -1;
         ctx = s_ctx[b];
         blk_lo = first_visible_block(ctx, wl);
         seg_f0 = cur.f;
@@ -509,141 +609,220 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
           }
         }
       }
-      // every wait is made warp-uniform: the tcgen05.ld/st that follow are
-      // warp-collective
-      ok = __all_sync(0xffffffffu,
-                      wait_bar(smem_u32(&bars.s_full[j & 1]), (uint32_t)((j >> 1) & 1), abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(tlane + (uint32_t)(j & 1) * kBN, sr[0]);
-      tmem_ld32(tlane + (uint32_t)(j & 1) * kBN + 32, sr[1]);
-      tmem_wait_ld();
-      const bool node = cur.u == cur.tiles - 1;
-      float s[64];
+      if ((int)(j & 1) == x) {
+        // every wait is made warp-uniform: the tcgen05.ld/st that follow are
+        // warp-collective
+        ok = __all_sync(0xffffffffu,
+                        wait_fast(smem_u32(&bars.s_full[x]), (uint32_t)((j >> 1) & 1), abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[2][32];
+        tmem_ld32(t_s, sr[0]);
+        tmem_ld32(t_s + 32, sr[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.s_free[x]));  // the S buffer may be refilled
+        const bool node = cur.u == cur.tiles - 1;
+        float s[64];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
-      // mask
-      if (!row_ok) {
+        for (int c = 0; c < 64; ++c) s[c] = __uint_as_float(sr[c >> 5][c & 31]);
+        if (!row_ok) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
-      } else if (node) {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c >= N || !((allowed >> c) & 1ull)) s[c] = -INFINITY;
-      } else {
-        const int kb = (blk_lo + 4 * cur.u) * kBlock;
-        int c0 = wl >= 0 ? pos_t - wl - kb : 0;
-        int c1 = ctx - kb;
-        if (c0 > 0 || c1 < 64) {
+          for (int c = 0; c < 64; ++c) s[c] = -INFINITY;
+        } else if (node) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
-            if (c < c0 || c >= c1) s[c] = -INFINITY;
+            if (c >= N || !((allowed >> c) & 1ull)) s[c] = -INFINITY;
+        } else {
+          const int kb = (blk_lo + 4 * cur.u) * kBlock;
+          const int c0 = wl >= 0 ? pos_t - wl - kb : 0;
+          const int c1 = ctx - kb;
+          if (c0 > 0 || c1 < 64) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (c < c0 || c >= c1) s[c] = -INFINITY;
+          }
         }
-      }
-      float mx = s[0];
+        float mt[16];
 #pragma unroll
-      for (int c = 1; c < 64; ++c) mx = fmaxf(mx, s[c]);
-      const float mxs = mx * qscale;
-      // Rescale O only when some row's max grew by more than 2^kTau.  The
-      // decision is made per warp (tcgen05.ld/st are warp-collective); rows that
-      // do not need it scale by 1.  A finite running max means an earlier tile
-      // of this segment exists, so PV_{j-1} is the last write to O.
-      const bool need = m_used != -INFINITY && mxs > m_used + kTau;
-      if (__any_sync(0xffffffffu, need)) {
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars.pv_done[(j - 1) & 1]),
-                                              (uint32_t)(((j - 1) >> 1) & 1), abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        const float alpha = need ? ex2(m_used - mxs) : 1.f;
+        for (int i = 0; i < 16; ++i)
+          mt[i] = fmaxf(fmaxf(s[i], s[i + 16]), fmaxf(s[i + 32], s[i + 48]));
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tlane + kColO + c * 32, o);
-          tmem_wait_ld();
+        for (int w = 8; w > 0; w >>= 1)
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tlane + kColO + c * 32, o);
+          for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
+        const float mxs = mt[0] * qscale;
+        // Rescale this warpgroup's O only when some row's max grew by more than
+        // 2^kTau; decided per warp (tcgen05.ld/st are warp-collective), rows
+        // that do not need it scale by 1.  A finite running max means this
+        // warpgroup had an earlier tile in the segment: PV_{j-2} wrote O last.
+        const bool need = m_used != -INFINITY && mxs > m_used + kTau;
+        if (j >= 2) {
+          // PV_{j-2} done: P buffer x is free and O_x is quiescent
+          ok = __all_sync(0xffffffffu, wait_fast(smem_u32(&bars.pv_done[x]),
+                                                 (uint32_t)(((j - 2) >> 1) & 1), abort_flag));
+          if (!ok) break;
         }
-        tmem_wait_st();
-        if (need) {
-          l *= alpha;
-          m_used = mxs;
-        }
-      }
-      if (m_used == -INFINITY) m_used = mxs;
-      // P = 2^(s*scale - m), written as bf16 into the 128B-swizzled P buffer
-      float rowsum = 0.f;
-      uint32_t pk[32];
-      const bool live = m_used != -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = live ? ex2(fmaf(s[c], qscale, -m_used)) : 0.f;
-        const float p1 = live ? ex2(fmaf(s[c + 1], qscale, -m_used)) : 0.f;
-        rowsum += p0 + p1;
-        pk[c >> 1] = pack_bf16(p0, p1);
-      }
-      l += rowsum;
-      if (j >= 2) {
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars.pv_done[j & 1]),
-                                              (uint32_t)(((j - 2) >> 1) & 1), abort_flag));
-        if (!ok) break;
-      }
-      const uint32_t pbuf = sbase + kOffP + (uint32_t)(j & 1) * kPBytes + p_row;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(pbuf + (((uint32_t)u ^ sw) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
-                     pk[4 * u + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full[j & 1]));
-      if (cur.seg_end()) {
-        // epilogue: wait for PV_j, read O, write output or partial
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(smem_u32(&bars.pv_done[j & 1]), (uint32_t)((j >> 1) & 1), abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        if (seg_complete) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          __nv_bfloat16 *dst =
-              p.out + (((size_t)b * N + t) * p.Hq + kvh * G + g) * kD;
-#pragma unroll
+        if (__any_sync(0xffffffffu, need)) {
+          tc_fence_after();
+          const float alpha = need ? ex2(m_used - mxs) : 1.f;
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
-            tmem_ld32(tlane + kColO + c * 32, o);
+            tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
-            if (row_ok) {
 #pragma unroll
-              for (int e = 0; e < 32; e += 8) {
-                uint4 w;
-                w.x = pack_bf16(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                w.y = pack_bf16(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                w.z = pack_bf16(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                w.w = pack_bf16(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c * 32, o);
+          }
+          tmem_wait_st();
+          if (need) {
+            l *= alpha;
+            m_used = mxs;
+          }
+        }
+        if (m_used == -INFINITY) m_used = mxs;
+        // a running max of -inf means every score so far is -inf: 2^(-inf) = 0
+        const float neg_m = m_used != -INFINITY ? -m_used : 0.f;
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2(fmaf(s[c], qscale, neg_m));
+          const float p1 = ex2(fmaf(s[c + 1], qscale, neg_m));
+          ps[(c >> 1) & 7] += p0 + p1;
+          pk[c >> 1] = pack_bf16(p0, p1);
+        }
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        // P_j as bf16 pairs into this warpgroup's P columns of TMEM (the A
+        // operand of the P V product): key 2c in the low half of column c
+        tmem_st32(t_p, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.p_full[x]));
+        // Once the warpgroup's P is complete one fixed thread of it issues
+        // O_x += P_j V_j.  A bounded mbarrier wait, not a named barrier: a warp
+        // that gave up must not leave the others blocked.  The issuing threads
+        // stay fixed (this one per warpgroup, plus the S issuer).
+        if (m == 0) {
+          bool go = wait_fast(smem_u32(&bars.p_full[x]), (uint32_t)((j >> 1) & 1), abort_flag);
+          if (go && last_j < 0 && x == 1 && seg > 0)  // O_1 must have been read out (merge)
+            go = wait_fast(smem_u32(&bars.o_free), (uint32_t)((seg - 1) & 1), abort_flag);
+          if (go) {
+            tc_fence_after();
+            const int stage = (int)(j % kStages);
+            const int nblk = (cur.u == cur.tiles - 1 ? NP : kBN) / 16;
+            const uint32_t ap = tmem + kColP + (uint32_t)x * 32;
+            const uint64_t bv = dv0 + (uint64_t)((stage * kStageBytes) >> 4);
+            const uint32_t od = tmem + kColO + (uint32_t)x * kD;
+            // 16 keys (one paged block) per instruction: V block i is
+            // [2 halves of d][16 keys][64 d], halves kBlkChunk apart (LBO),
+            // 8-key groups 1024 B apart (SBO)
+            for (int i = 0; i < nblk; ++i)
+              umma_f16_ta(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
+                          (i > 0 || last_j >= 0) ? 1u : 0u);
+            umma_commit(smem_u32(&bars.pv_done[x]));
+            umma_commit(smem_u32(&bars.kv_empty[stage]));
+          } else {
+            *abort_flag = 1;
+          }
+        }
+        last_j = j;
+      }
+      if (cur.seg_end()) {
+        // this warpgroup's last PV of the segment must have landed in O_x
+        if (last_j >= 0) {
+          ok = __all_sync(0xffffffffu, wait_fast(smem_u32(&bars.pv_done[x]),
+                                                 (uint32_t)((last_j >> 1) & 1), abort_flag));
+          if (!ok) break;
+        }
+        float2 *mrg = reinterpret_cast<float2 *>(smem + kOffMerge) + (seg & 1) * kM;
+        if (x == 1) {
+          // hand (max, sum) to warpgroup 0; wait until it consumed the previous
+          // segment's hand-over so the two never drift more than one apart
+          if (seg > 0) {
+            ok = __all_sync(0xffffffffu,
+                            wait_fast(smem_u32(&bars.o_free), (uint32_t)((seg - 1) & 1), abort_flag));
+            if (!ok) break;
+          }
+          mrg[m] = make_float2(m_used, l);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.merge));
+        } else {
+          ok = __all_sync(0xffffffffu,
+                          wait_fast(smem_u32(&bars.merge), (uint32_t)(seg & 1), abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          const float2 other = mrg[m];
+          const float M = fmaxf(m_used, other.x);
+          const float w0 = m_used == -INFINITY ? 0.f : ex2(m_used - M);
+          const float w1 = other.x == -INFINITY ? 0.f : ex2(other.x - M);
+          const float L = l * w0 + other.y * w1;
+          const uint32_t t_o0 = tlane + kColO, t_o1 = tlane + kColO + kD;
+          if (seg_complete) {
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            const float a0 = w0 * inv, a1 = w1 * inv;
+            __nv_bfloat16 *dst = p.out + (((size_t)b * N + t) * p.Hq + kvh * G + g) * kD;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o0[32], o1[32];
+              tmem_ld32(t_o0 + c * 32, o0);
+              tmem_ld32(t_o1 + c * 32, o1);
+              tmem_wait_ld();
+              if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                  float v[8];
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) {
+                    const float f0 = w0 > 0.f ? __uint_as_float(o0[e + k]) * a0 : 0.f;
+                    const float f1 = w1 > 0.f ? __uint_as_float(o1[e + k]) * a1 : 0.f;
+                    v[k] = f0 + f1;
+                  }
+                  uint4 w;
+                  w.x = pack_bf16(v[0], v[1]);
+                  w.y = pack_bf16(v[2], v[3]);
+                  w.z = pack_bf16(v[4], v[5]);
+                  w.w = pack_bf16(v[6], v[7]);
+                  *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
+                }
               }
             }
-          }
-        } else {
-          const int slot = 2 * (int)blockIdx.x + (seg_f0 == lo ? 0 : 1);
-          float *dst = tp.part_o + ((size_t)slot * kM + m) * kD;
+          } else {
+            const int slot = 2 * (int)blockIdx.x + (seg_f0 == lo ? 0 : 1);
+            float *dst = tp.part_o + ((size_t)slot * kM + m) * kD;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o0[32], o1[32];
+              tmem_ld32(t_o0 + c * 32, o0);
+              tmem_ld32(t_o1 + c * 32, o1);
+              tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tlane + kColO + c * 32, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<uint4 *>(dst + c * 32 + e) = make_uint4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+              for (int e = 0; e < 32; e += 4) {
+                float4 v;
+                v.x = (w0 > 0.f ? __uint_as_float(o0[e]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e]) * w1 : 0.f);
+                v.y = (w0 > 0.f ? __uint_as_float(o0[e + 1]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 1]) * w1 : 0.f);
+                v.z = (w0 > 0.f ? __uint_as_float(o0[e + 2]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 2]) * w1 : 0.f);
+                v.w = (w0 > 0.f ? __uint_as_float(o0[e + 3]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 3]) * w1 : 0.f);
+                *reinterpret_cast<float4 *>(dst + c * 32 + e) = v;
+              }
+            }
+            tp.part_ml[(size_t)slot * kM + m] = make_float2(M, L);
           }
-          tp.part_ml[(size_t)slot * kM + m] = make_float2(m_used, l);
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.o_free));
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars.o_free));
         ++seg;
       }
       ++j;
       cur.next();
+    }
+    if (m == 0) {
+      // the commits this thread issued (pv_done, kv_empty) have all landed once
+      // this one has: nothing arrives on shared memory after the CTA exits
+      umma_commit(smem_u32(&bars.fin_pv[x]));
+      int dummy = 0;
+      wait_bar(smem_u32(&bars.fin_pv[x]), 0, &dummy);
     }
     if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
   }
@@ -725,7 +904,7 @@ bool make_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
               const uint64_t *strides, const uint32_t *box) {
   auto fn = encode_fn();
   if (!fn) return false;
-  const uint32_t estr[3] = {1, 1, 1};
+  const uint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
             reinterpret_cast<const cuuint64_t *>(dims), reinterpret_cast<const cuuint64_t *>(strides),
             reinterpret_cast<const cuuint32_t *>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -762,26 +941,39 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   CUtensorMap mq, mkc, mvc, mkcr, mvcr, mkt, mvt;
   const uint64_t row_bytes = kD * 2;
   {
+    // Q [B*N][Hq][128]: box = the G heads x N nodes of one KV head, one d half
     const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.N};
     const uint64_t str[2] = {row_bytes, row_bytes * a.Hq};
     const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)a.N};
     if (!make_map(&mq, a.q, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
+    // cache rows (block, head, token) of 128 d, viewed as [d half][row][64]:
+    // one copy moves a whole 16-token block as [2][16][64]
     const uint64_t rows = (uint64_t)(a.num_blocks > 0 ? a.num_blocks : 1) * a.Hkv * kBlock;
-    const uint64_t dims[2] = {(uint64_t)kD, rows};
-    const uint64_t str[1] = {row_bytes};
-    const uint32_t box[2] = {64, (uint32_t)kBlock};
+    const uint64_t dims3[3] = {64, rows, 2};
+    const uint64_t str3[2] = {row_bytes, 128};
+    const uint32_t box3[3] = {64, (uint32_t)kBlock, 2};
+    const uint64_t dims2[2] = {(uint64_t)kD, rows};
+    const uint64_t str2[1] = {row_bytes};
+    const uint32_t box16[2] = {64, (uint32_t)kBlock};
     const uint32_t box1[2] = {64, 1};
-    if (!make_map(&mkc, a.k_cache, 2, dims, str, box) || !make_map(&mvc, a.v_cache, 2, dims, str, box) ||
-        !make_map(&mkcr, a.k_cache, 2, dims, str, box1) || !make_map(&mvcr, a.v_cache, 2, dims, str, box1))
+    if (!make_map(&mkc, a.k_cache, 2, dims2, str2, box16) ||
+        !make_map(&mvc, a.v_cache, 3, dims3, str3, box3) ||
+        !make_map(&mkcr, a.k_cache, 2, dims2, str2, box1) ||
+        !make_map(&mvcr, a.v_cache, 2, dims2, str2, box1))
       return cudaErrorInvalidValue;
   }
   {
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.N};
-    const uint64_t str[2] = {row_bytes, row_bytes * a.Hkv};
-    const uint32_t box[3] = {64, 1, (uint32_t)a.N};
-    if (!make_map(&mkt, a.k_tree, 3, dims, str, box) || !make_map(&mvt, a.v_tree, 3, dims, str, box))
+    // tree K [B*N][Hkv][128]: 16 consecutive nodes of one head, one d half;
+    // tree V viewed as [d half][node][head][64]: 16 nodes as [2][16][64]
+    const uint64_t dimsk[3] = {(uint64_t)kD, (uint64_t)a.Hkv, (uint64_t)a.B * a.N};
+    const uint64_t strk[2] = {row_bytes, row_bytes * a.Hkv};
+    const uint32_t boxk[3] = {64, 1, 16};
+    const uint64_t dims[4] = {64, (uint64_t)a.Hkv, (uint64_t)a.B * a.N, 2};
+    const uint64_t str[3] = {row_bytes, row_bytes * a.Hkv, 128};
+    const uint32_t box[4] = {64, 1, 16, 2};
+    if (!make_map(&mkt, a.k_tree, 3, dimsk, strk, boxk) || !make_map(&mvt, a.v_tree, 4, dims, str, box))
       return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
