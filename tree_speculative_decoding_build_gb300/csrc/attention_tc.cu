@@ -16,7 +16,8 @@
 //              one more tile per segment.
 //   warp 1     TMEM allocation and the single MMA-issuing thread:
 //              S_j = Q K_j^T into a double-buffered TMEM S tile, then
-//              O += P_j V_j (V read as an MN-major operand) into TMEM O.
+//              O += P_j V_j (P from TMEM, V read as an MN-major operand).
+//              Every tcgen05.mma of the CTA is issued by this one thread.
 //   warps 2-5  softmax: thread r owns row r; reads S_j from TMEM, applies the
 //              context / window / ancestor mask, keeps the running max and sum,
 //              writes P_j (bf16 pairs) to TMEM, where the P V product reads it.  O is rescaled in
@@ -90,7 +91,6 @@ struct Bars {
   unsigned long long merge;
   unsigned long long o_free;
   unsigned long long fin;
-  unsigned long long fin_pv[2];
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -264,8 +264,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     mbar_init(smem_u32(&bars.merge), 128);
     mbar_init(smem_u32(&bars.o_free), 128);
     mbar_init(smem_u32(&bars.fin), 1);
-    mbar_init(smem_u32(&bars.fin_pv[0]), 1);
-    mbar_init(smem_u32(&bars.fin_pv[1]), 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -513,51 +511,126 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
     }
   } else if (warp == 1) {
-    // ======================================================== S issuer
-    // One thread issues S_j = Q K_j^T for every tile in order: it needs the
-    // K tile, Q of the segment, and the S buffer (j&1) read out by the softmax
-    // (s_free of tile j-2, signalled right after the softmax loaded S, so S of
-    // the next tile is computed while the softmax still works on the current
-    // one).  The P V products are issued by the softmax warpgroups themselves.
-    if (lane == 0) {
+    // ======================================================== MMA issuer
+    // The only warp that issues tcgen05.mma (one lane per instruction, chosen
+    // by elect.sync).  The whole warp runs this loop with warp-uniform control
+    // flow (barrier tests are votes), so operands stay warp-uniform.  It polls
+    // for whichever MMA can go next, PV first (it releases a stage), then S,
+    // so a late K/V tile never holds up a ready P V product.
+    //   S_j  needs its K tile, Q of its segment, and S buffer j&1 read out by
+    //        the softmax (s_free of tile j-2, signalled right after the softmax
+    //        loaded S, so S of the next tile is ready before it is needed).
+    //   PV_k needs P_k (p_full) and, for the first PV of a segment, the
+    //        previous segment's O read out by the merge (o_free).
+    {
+      const uint32_t idesc_pv = make_idesc(kM, kD, true);
+      // descriptors: start-address field = address >> 4, so byte offsets
+      // (below 256 KB) are added as offset >> 4
       const uint64_t dq = sw128_desc(sbase + kOffQ, 16, 1024);
       const uint64_t dk = sw128_desc(sbase + kOffKV, 16, 1024);
-      bool ok = true;
-      int js = 0;
-      int seg = 0;
-      while (ok && cur.valid()) {
-        const bool first = cur.seg_start(lo);
-        const int stage = js % kStages;
-        if (js >= 2)
-          ok = wait_fast(smem_u32(&bars.s_free[js & 1]), (uint32_t)(((js - 2) >> 1) & 1), abort_flag);
-        if (ok && first) ok = wait_fast(smem_u32(&bars.q_full), (uint32_t)(seg & 1), abort_flag);
-        if (ok) ok = wait_fast(smem_u32(&bars.kv_full[stage]), (uint32_t)((js / kStages) & 1), abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        if (first) ++seg;
-        const bool last = cur.seg_end();
-        const int keys = cur.u == cur.tiles - 1 ? NP : kBN;
-        const uint32_t idesc_s = make_idesc(kM, keys, false);
-        // start-address field = address >> 4: byte offsets are added as offset >> 4
-        const uint64_t bk = dk + (uint64_t)((stage * kStageBytes) >> 4);
-        const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
-        // Q and K are [2 d halves][rows][64], 128-byte swizzled
+      const uint64_t dv = sw128_desc(sbase + kOffKV + kHalfStage, kBlkChunk, 1024);
+      // S issued, PV not yet: at most kStages tiles (S_j waits for the stage
+      // PV_{j-kStages} released).  Packed: blocks | seg_first << 3 |
+      // acc_first << 4 | segment << 5, shifted out as PVs are issued.
+      uint32_t pend[kStages];
 #pragma unroll
-        for (int ks = 0; ks < kD / 16; ++ks) {
-          const uint32_t off_q = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
-          const uint32_t off_k = ((ks >> 2) * kKVChunk + (ks & 3) * 32) >> 4;
-          umma_f16(sc, dq + off_q, bk + off_k, idesc_s, ks > 0 ? 1u : 0u);
+      for (int i = 0; i < kStages; ++i) pend[i] = 0;
+      bool ok = true;
+      int js = 0, jp = 0, seg = 0;
+      bool ostart0 = false, ostart1 = false;
+      uint64_t t0 = 0;
+      for (uint32_t spin = 0;; ++spin) {
+        bool progressed = false;
+        if (jp < js) {
+          const uint32_t mt = pend[0];
+          const int m_seg = (int)(mt >> 5);
+          const bool m_first = (mt >> 3) & 1;
+          if (__all_sync(0xffffffffu,
+                         mbar_test_wait(smem_u32(&bars.p_full[jp & 1]), (uint32_t)((jp >> 1) & 1)) &&
+                             (!m_first || m_seg == 0 ||
+                              mbar_test_wait(smem_u32(&bars.o_free), (uint32_t)((m_seg - 1) & 1))))) {
+            tc_fence_after();
+            const int x = jp & 1;
+            const int stage = jp % kStages;
+            const uint32_t nblk = mt & 7;
+            const bool acc_first = (mt >> 4) & 1;
+            const uint32_t ap = tmem + kColP + (uint32_t)x * 32;
+            const uint64_t bv = dv + (uint64_t)((stage * kStageBytes) >> 4);
+            const uint32_t od = tmem + kColO + (uint32_t)x * kD;
+            // 16 keys (one paged block) per instruction: A = P from TMEM (8
+            // columns of bf16 pairs), V block i is [2 d halves][16 keys][64 d],
+            // halves kBlkChunk apart (LBO), 8-key groups 1024 B apart (SBO)
+            for (uint32_t i = 0; i < nblk; ++i)
+              umma_f16_ta_warp(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
+                               (i > 0 || !acc_first) ? 1u : 0u);
+            umma_commit_warp(smem_u32(&bars.pv_done[x]));
+            umma_commit_warp(smem_u32(&bars.kv_empty[stage]));
+#pragma unroll
+            for (int i = 0; i + 1 < kStages; ++i) pend[i] = pend[i + 1];
+            ++jp;
+            progressed = true;
+          }
         }
-        umma_commit(smem_u32(&bars.s_full[js & 1]));
-        if (last) umma_commit(smem_u32(&bars.q_empty));
-        ++js;
-        cur.next();
+        if (cur.valid()) {
+          const bool first = cur.seg_start(lo);
+          const int stage = js % kStages;
+          if (__all_sync(0xffffffffu,
+                         (js < 2 || mbar_test_wait(smem_u32(&bars.s_free[js & 1]),
+                                                   (uint32_t)(((js - 2) >> 1) & 1))) &&
+                             (!first || mbar_test_wait(smem_u32(&bars.q_full), (uint32_t)(seg & 1))) &&
+                             mbar_test_wait(smem_u32(&bars.kv_full[stage]),
+                                            (uint32_t)((js / kStages) & 1)))) {
+            tc_fence_after();
+            if (first) {
+              ++seg;
+              ostart0 = ostart1 = false;
+            }
+            const int keys = cur.u == cur.tiles - 1 ? NP : kBN;
+            const uint32_t idesc_s = make_idesc(kM, keys, false);
+            const uint64_t bk = dk + (uint64_t)((stage * kStageBytes) >> 4);
+            const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
+            // Q and K are [2 d halves][rows][64], 128-byte swizzled
+#pragma unroll
+            for (int ks = 0; ks < kD / 16; ++ks) {
+              const uint32_t off_q = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
+              const uint32_t off_k = ((ks >> 2) * kKVChunk + (ks & 3) * 32) >> 4;
+              umma_f16_warp(sc, dq + off_q, bk + off_k, idesc_s, ks > 0 ? 1u : 0u);
+            }
+            umma_commit_warp(smem_u32(&bars.s_full[js & 1]));
+            if (cur.seg_end()) umma_commit_warp(smem_u32(&bars.q_empty));
+            const bool par = js & 1;
+            const bool acc_first = par ? !ostart1 : !ostart0;
+            if (par) ostart1 = true;
+            else ostart0 = true;
+            const uint32_t mt = (uint32_t)(keys >> 4) | ((uint32_t)first << 3) |
+                                ((uint32_t)acc_first << 4) | ((uint32_t)(seg - 1) << 5);
+#pragma unroll
+            for (int i = 0; i < kStages; ++i)
+              if (i == js - jp) pend[i] = mt;
+            ++js;
+            cur.next();
+            progressed = true;
+          }
+        }
+        if (!cur.valid() && jp == js) break;
+        if (progressed) {
+          t0 = 0;
+        } else if ((spin & 63) == 63) {
+          const uint64_t now = globaltimer();
+          if (t0 == 0) t0 = now;
+          const bool give_up = __any_sync(0xffffffffu, *abort_flag != 0 || now - t0 > kWaitNs);
+          if (give_up) {
+            if (lane == 0) *abort_flag = 1;
+            ok = false;
+            break;
+          }
+        }
       }
       // every MMA issued so far has completed once this arrives
-      umma_commit(smem_u32(&bars.fin));
+      umma_commit_warp(smem_u32(&bars.fin));
       int dummy = 0;
       wait_bar(smem_u32(&bars.fin), 0, &dummy);
-      if (!ok) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
+      if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
     }
   } else {
     // ======================================================== softmax / epilogue
@@ -585,8 +658,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     long long seg_f0 = lo;
     bool seg_complete = false;
     const uint32_t t_p = tlane + kColP + (uint32_t)x * 32;
-    const uint32_t idesc_pv = make_idesc(kM, kD, true);
-    const uint64_t dv0 = sw128_desc(sbase + kOffKV + kHalfStage, kBlkChunk, 1024);
     while (cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
       if (cur.seg_start(lo)) {
@@ -699,34 +770,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tmem_st32(t_p, pk);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.p_full[x]));
-        // Once the warpgroup's P is complete one fixed thread of it issues
-        // O_x += P_j V_j.  A bounded mbarrier wait, not a named barrier: a warp
-        // that gave up must not leave the others blocked.  The issuing threads
-        // stay fixed (this one per warpgroup, plus the S issuer).
-        if (m == 0) {
-          bool go = wait_fast(smem_u32(&bars.p_full[x]), (uint32_t)((j >> 1) & 1), abort_flag);
-          if (go && last_j < 0 && x == 1 && seg > 0)  // O_1 must have been read out (merge)
-            go = wait_fast(smem_u32(&bars.o_free), (uint32_t)((seg - 1) & 1), abort_flag);
-          if (go) {
-            tc_fence_after();
-            const int stage = (int)(j % kStages);
-            const int nblk = (cur.u == cur.tiles - 1 ? NP : kBN) / 16;
-            const uint32_t ap = tmem + kColP + (uint32_t)x * 32;
-            const uint64_t bv = dv0 + (uint64_t)((stage * kStageBytes) >> 4);
-            const uint32_t od = tmem + kColO + (uint32_t)x * kD;
-            // 16 keys (one paged block) per instruction: V block i is
-            // [2 halves of d][16 keys][64 d], halves kBlkChunk apart (LBO),
-            // 8-key groups 1024 B apart (SBO)
-            for (int i = 0; i < nblk; ++i)
-              umma_f16_ta(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
-                          (i > 0 || last_j >= 0) ? 1u : 0u);
-            umma_commit(smem_u32(&bars.pv_done[x]));
-            umma_commit(smem_u32(&bars.kv_empty[stage]));
-          } else {
-            *abort_flag = 1;
-          }
-        }
+        mbar_arrive(smem_u32(&bars.p_full[x]));  // the MMA thread issues O_x += P_j V_j
         last_j = j;
       }
       if (cur.seg_end()) {
@@ -816,13 +860,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       ++j;
       cur.next();
-    }
-    if (m == 0) {
-      // the commits this thread issued (pv_done, kv_empty) have all landed once
-      // this one has: nothing arrives on shared memory after the CTA exits
-      umma_commit(smem_u32(&bars.fin_pv[x]));
-      int dummy = 0;
-      wait_bar(smem_u32(&bars.fin_pv[x]), 0, &dummy);
     }
     if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
   }
