@@ -48,25 +48,24 @@ using namespace ptx;
 constexpr int kD = 128;
 constexpr int kM = 128;                 // UMMA M: rows per tile
 constexpr int kBN = 64;                 // keys per context tile (4 paged blocks)
-constexpr int kStages = 5;
+constexpr int kStages = 6;
 constexpr int kWarps = 11;               // producer, S issuer, 2 softmax warpgroups, producer
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxB = 1024;             // sequences the in-CTA schedule can hold
-constexpr uint32_t kQChunk = kM * 64 * 2;              // [128 rows][64 d] bf16 = 16 KB
 constexpr uint32_t kKVChunk = kBN * 64 * 2;            // [64 keys][64 d] bf16 = 8 KB
 constexpr uint32_t kStageBytes = 4 * kKVChunk;         // K (16 KB) + V (16 KB)
 constexpr uint32_t kHalfStage = 2 * kKVChunk;          // V starts here within a stage
 constexpr uint32_t kBlkChunk = kBlock * 64 * 2;        // [16 keys][64 d] bf16 = 2 KB
 constexpr uint32_t kBlkBytes = 2 * kBlkChunk;          // one paged block: [2 halves][16][64]
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = 2 * kQChunk;
+constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffPre = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffCtx = kOffPre + 4 * (kMaxB + 1);
 constexpr uint32_t kOffMerge = (kOffCtx + 4 * kMaxB + 15) / 16 * 16;   // [2][128] float2
 constexpr uint32_t kSmemBytes = kOffMerge + 2 * kM * 8 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = 512;     // S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448)
+constexpr uint32_t kTmemCols = 512;     // S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448); Q [448,512)
 constexpr uint32_t kColO = 128;
 constexpr uint32_t kColP = 384;         // P as bf16 pairs: 64 keys = 32 columns
+constexpr uint32_t kColQ = 448;         // Q as bf16 pairs: 128 dims = 64 columns
 constexpr float kTau = 8.0f;            // rescale O only when the max grows by > 2^8
 constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait at most
 
@@ -181,7 +180,7 @@ __device__ __forceinline__ int ctx_tiles(int ctx, int window_left) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
                const __grid_constant__ CUtensorMap tm_vc,
                const __grid_constant__ CUtensorMap tm_kc_row,
                const __grid_constant__ CUtensorMap tm_vc_row,
@@ -217,15 +216,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     s_pre[0] = 0;
     s_abort = 0;
   }
-  // zero the Q rows no TMA ever writes (R < 128)
-  if (R < kM) {
-    const int words = (kM - R) * 8;  // 16-byte words per chunk
-    for (int i = tid; i < 2 * words; i += kThreads) {
-      const int c = i / words, w = i - c * words;
-      *reinterpret_cast<uint4 *>(smem + kOffQ + c * kQChunk + R * 128 + w * 16) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();
-  }
   __syncthreads();
   if (warp == 0) {  // inclusive scan of s_pre[1..B]
     const int per = (B + 31) / 32;
@@ -253,7 +243,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       mbar_init(smem_u32(&bars.kv_full[s]), 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars.q_full), 1);
+    mbar_init(smem_u32(&bars.q_full), 128);
     mbar_init(smem_u32(&bars.q_empty), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars.s_full[i]), 1);
@@ -289,7 +279,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     // the tiles of the other.
     const int par = warp == 0 ? 0 : 1;
     if (lane == 0 && par == 0) {
-      prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_kc);
       prefetch_tensormap(&tm_vc);
       prefetch_tensormap(&tm_kt);
@@ -297,32 +286,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
     int j = 0;
     int seg = 0;
-    int q_pending = -1, q_b = 0, q_kvh = 0;  // segment whose Q copy is not issued yet
     int ctx = 0, blk_lo = 0, nblk_end = 0, nfull = 0;
     int win_base = 0, cur_id = -1, nxt_id = -1;
     bool ok = true;
     auto load_id = [&](int b, int slot) -> int {
       return slot < nblk_end ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
     };
-    auto issue_q = [&]() {
-      if (lane == 0) {
-        const uint32_t qb = smem_u32(&bars.q_full);
-        mbar_arrive_expect_tx(qb, 2u * R * 128u);
-        tma_load_3d(sbase + kOffQ, &tm_q, qb, 0, q_kvh * G, q_b * N);
-        tma_load_3d(sbase + kOffQ + kQChunk, &tm_q, qb, 64, q_kvh * G, q_b * N);
-      }
-      q_pending = -1;
-    };
     while (ok && cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
       if (cur.seg_start(lo)) {
-        if (q_pending >= 0) {  // the previous segment's Q is still waiting: finish it first
-          if (lane == 0 && q_pending > 0)
-            ok = wait_fast(smem_u32(&bars.q_empty), (q_pending - 1) & 1, abort_flag);
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          issue_q();
-        }
         ctx = s_ctx[b];
         blk_lo = first_visible_block(ctx, p.window_left);
         nblk_end = (ctx + kBlock - 1) / kBlock;
@@ -330,11 +302,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         win_base = blk_lo + 4 * cur.u;  // a CTA's range may start mid-pair
         cur_id = load_id(b, win_base + lane);
         nxt_id = load_id(b, win_base + 32 + lane);
-        if (par == 0) {
-          q_pending = seg;
-          q_b = b;
-          q_kvh = kvh;
-        }
         ++seg;
       }
       const int nct = cur.tiles - 1;
@@ -351,45 +318,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       }
       const int stage = j % kStages;
       const uint32_t empty_parity = (uint32_t)((j / kStages - 1) & 1);
-      if (q_pending < 0) {
-        // common case: every lane waits for the stage itself (no broadcasts)
-        if (j >= kStages) {
-          ok = __all_sync(0xffffffffu,
-                          wait_fast(smem_u32(&bars.kv_empty[stage]), empty_parity, abort_flag));
-          if (!ok) break;
-        }
-      } else {
-        // acquire the stage, issuing the pending Q copy as soon as Q is free
-        bool got = j < kStages;
-        uint64_t t0 = 0;
-        for (uint32_t spin = 0;; ++spin) {
-          int qr = 0, gr = got;
-          if (lane == 0) {
-            if (q_pending >= 0)
-              qr = q_pending == 0 || mbar_test_wait(smem_u32(&bars.q_empty), (q_pending - 1) & 1);
-            if (!gr) gr = mbar_test_wait(smem_u32(&bars.kv_empty[stage]), empty_parity);
-          }
-          qr = __shfl_sync(0xffffffffu, qr, 0);
-          gr = __shfl_sync(0xffffffffu, gr, 0);
-          if (qr) issue_q();
-          got = gr;
-          if (got) break;
-          if ((spin & 63) == 63) {
-            int bad = 0;
-            if (lane == 0) {
-              const uint64_t now = globaltimer();
-              if (t0 == 0) t0 = now;
-              if (*abort_flag || now - t0 > kWaitNs) {
-                *abort_flag = 1;
-                bad = 1;
-              }
-            }
-            if (__shfl_sync(0xffffffffu, bad, 0)) {
-              ok = false;
-              break;
-            }
-          }
-        }
+      // every lane waits for the stage itself (no broadcasts)
+      if (j >= kStages) {
+        ok = __all_sync(0xffffffffu,
+                        wait_fast(smem_u32(&bars.kv_empty[stage]), empty_parity, abort_flag));
         if (!ok) break;
       }
       unsigned char *st = smem + kOffKV + stage * kStageBytes;
@@ -496,18 +428,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       ++j;
       cur.next();
     }
-    if (ok && q_pending >= 0) {  // the last segment's Q: the MMA is waiting for it
-      if (lane == 0 && q_pending > 0)
-        ok = wait_fast(smem_u32(&bars.q_empty), (q_pending - 1) & 1, abort_flag);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (ok) issue_q();
-    }
     if (!ok && lane == 0) {
       // give copies still in flight a bounded chance to land before exit
       int dummy = 0;
       for (int k = j > kStages ? j - kStages : 0; k < j; ++k)
         if ((k & 1) == par) wait_bar(smem_u32(&bars.kv_full[k % kStages]), (uint32_t)((k / kStages) & 1), &dummy);
-      if (par == 0 && seg > 0) wait_bar(smem_u32(&bars.q_full), (seg - 1) & 1, &dummy);
       set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
     }
   } else if (warp == 1) {
@@ -526,7 +451,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
       const uint32_t idesc_pv = make_idesc(kM, kD, true);
       // descriptors: start-address field = address >> 4, so byte offsets
       // (below 256 KB) are added as offset >> 4
-      const uint64_t dq = sw128_desc(sbase + kOffQ, 16, 1024);
       const uint64_t dk = sw128_desc(sbase + kOffKV, 16, 1024);
       const uint64_t dv = sw128_desc(sbase + kOffKV + kHalfStage, kBlkChunk, 1024);
       // S issued, PV not yet: at most kStages tiles (S_j waits for the stage
@@ -560,11 +484,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // 16 keys (one paged block) per instruction: A = P from TMEM (8
             // columns of bf16 pairs), V block i is [2 d halves][16 keys][64 d],
             // halves kBlkChunk apart (LBO), 8-key groups 1024 B apart (SBO)
-            for (uint32_t i = 0; i < nblk; ++i)
-              umma_f16_ta_warp(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
-                               (i > 0 || !acc_first) ? 1u : 0u);
-            umma_commit_warp(smem_u32(&bars.pv_done[x]));
-            umma_commit_warp(smem_u32(&bars.kv_empty[stage]));
+            if (nblk == 4) {
+              umma_pv4_warp(od, ap, bv, kBlkBytes >> 4, idesc_pv, acc_first ? 0u : 1u,
+                            smem_u32(&bars.pv_done[x]), smem_u32(&bars.kv_empty[stage]));
+            } else {
+              for (uint32_t i = 0; i < nblk; ++i)
+                umma_f16_ta_warp(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
+                                 (i > 0 || !acc_first) ? 1u : 0u);
+              umma_commit_warp(smem_u32(&bars.pv_done[x]));
+              umma_commit_warp(smem_u32(&bars.kv_empty[stage]));
+            }
 #pragma unroll
             for (int i = 0; i + 1 < kStages; ++i) pend[i] = pend[i + 1];
             ++jp;
@@ -589,14 +518,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const uint32_t idesc_s = make_idesc(kM, keys, false);
             const uint64_t bk = dk + (uint64_t)((stage * kStageBytes) >> 4);
             const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
-            // Q and K are [2 d halves][rows][64], 128-byte swizzled
-#pragma unroll
-            for (int ks = 0; ks < kD / 16; ++ks) {
-              const uint32_t off_q = ((ks >> 2) * kQChunk + (ks & 3) * 32) >> 4;
-              const uint32_t off_k = ((ks >> 2) * kKVChunk + (ks & 3) * 32) >> 4;
-              umma_f16_warp(sc, dq + off_q, bk + off_k, idesc_s, ks > 0 ? 1u : 0u);
-            }
-            umma_commit_warp(smem_u32(&bars.s_full[js & 1]));
+            // A = Q from TMEM (bf16 pairs, 8 columns per 16 dims); K is
+            // [2 d halves][keys][64], 128-byte swizzled
+            umma_s_tile_warp(sc, tmem + kColQ, bk, kKVChunk >> 4, idesc_s, smem_u32(&bars.s_full[js & 1]));
             if (cur.seg_end()) umma_commit_warp(smem_u32(&bars.q_empty));
             const bool par = js & 1;
             const bool acc_first = par ? !ostart1 : !ostart0;
@@ -668,6 +592,31 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         blk_lo = first_visible_block(ctx, wl);
         seg_f0 = cur.f;
         seg_complete = cur.u == 0 && cur.f + (cur.tiles - 1) <= hi - 1;
+        if (x == 0) {
+          // Q rows of this (sequence, KV head) into TMEM once the previous
+          // segment's last S has read the old ones; rows past R are zero
+          if (seg > 0) {
+            ok = __all_sync(0xffffffffu,
+                            wait_fast(smem_u32(&bars.q_empty), (uint32_t)((seg - 1) & 1), abort_flag));
+            if (!ok) break;
+          }
+          uint32_t qr[2][32];
+          const uint4 *src = reinterpret_cast<const uint4 *>(
+              p.q + (((size_t)b * N + t) * p.Hq + kvh * G + g) * kD);
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            const uint4 w = row_ok ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+            qr[v >> 3][(v & 7) * 4 + 0] = w.x;
+            qr[v >> 3][(v & 7) * 4 + 1] = w.y;
+            qr[v >> 3][(v & 7) * 4 + 2] = w.z;
+            qr[v >> 3][(v & 7) * 4 + 3] = w.w;
+          }
+          tmem_st32(tlane + kColQ, qr[0]);
+          tmem_st32(tlane + kColQ + 32, qr[1]);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.q_full));
+        }
         allowed = 0;
         if (row_ok) {
           pos_t = p.pos[(size_t)b * N + t];
@@ -975,15 +924,8 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   tp.part_o = reinterpret_cast<float *>(ws);
   tp.node_pad = (a.N + 15) / 16 * 16;
 
-  CUtensorMap mq, mkc, mvc, mkcr, mvcr, mkt, mvt;
+  CUtensorMap mkc, mvc, mkcr, mvcr, mkt, mvt;
   const uint64_t row_bytes = kD * 2;
-  {
-    // Q [B*N][Hq][128]: box = the G heads x N nodes of one KV head, one d half
-    const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)a.Hq, (uint64_t)a.B * a.N};
-    const uint64_t str[2] = {row_bytes, row_bytes * a.Hq};
-    const uint32_t box[3] = {64, (uint32_t)a.G, (uint32_t)a.N};
-    if (!make_map(&mq, a.q, 3, dims, str, box)) return cudaErrorInvalidValue;
-  }
   {
     // cache rows (block, head, token) of 128 d, viewed as [d half][row][64]:
     // one copy moves a whole 16-token block as [2][16][64]
@@ -1016,7 +958,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<P, kThreads, kSmemBytes, stream>>>(mq, mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
+  attn_tc_kernel<<<P, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long rows = (long long)a.B * a.Hkv * a.R;

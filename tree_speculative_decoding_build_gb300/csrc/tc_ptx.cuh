@@ -161,6 +161,69 @@ __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
       : "memory");
 }
 
+// S = Q K^T for a 64-key (or 16/32/48-key node) tile from a converged warp:
+// eight K=16 steps over head dim 128, A = Q from TMEM (8 columns per step),
+// B = K from shared memory: [2 d halves][keys][64], 128-byte swizzled, halves
+// `half_off16` (bytes >> 4) apart, 32-byte steps within a half.  One lane
+// (elect.sync) issues the eight MMAs and the commit to `bar`.
+__device__ __forceinline__ void umma_s_tile_warp(uint32_t d_tmem, uint32_t q_tmem, uint64_t kdesc,
+                                                 uint32_t half_off16, uint32_t idesc, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e, f, t;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      ".reg .b64 h;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 f, %4, %4;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "cvt.u64.u32 h, %3;\n\t"
+      "add.s64 b1, %2, 2;\n\t"
+      "add.s64 b2, %2, 4;\n\t"
+      "add.s64 b3, %2, 6;\n\t"
+      "add.s64 b4, %2, h;\n\t"
+      "add.s64 b5, b4, 2;\n\t"
+      "add.s64 b6, b4, 4;\n\t"
+      "add.s64 b7, b4, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, f;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], b1, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], b2, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], b3, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], b4, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], b5, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], b6, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%11], b7, %4, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}" ::"r"(d_tmem),
+      "r"(q_tmem), "l"(kdesc), "r"(half_off16), "r"(idesc), "r"(q_tmem + 8), "r"(q_tmem + 16),
+      "r"(q_tmem + 24), "r"(q_tmem + 32), "r"(q_tmem + 40), "r"(q_tmem + 48), "r"(q_tmem + 56),
+      "r"(bar)
+      : "memory");
+}
+
+// O (+)= P V for a 64-key tile (four 16-key blocks) from a converged warp:
+// A = P from TMEM (8 columns per block), B = V block i at `vdesc` + i * blk16
+// (descriptor units).  `acc0` = 0 starts O afresh.  One lane issues the MMAs
+// and the commits to `bar0` and `bar1`.
+__device__ __forceinline__ void umma_pv4_warp(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                              uint32_t blk16, uint32_t idesc, uint32_t acc0,
+                                              uint32_t bar0, uint32_t bar1) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t;\n\t.reg .b64 v1, v2, v3, s;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.eq.b32 t, %5, %5;\n\t"
+      "cvt.u64.u32 s, %3;\n\t"
+      "add.s64 v1, %2, s;\n\t"
+      "add.s64 v2, v1, s;\n\t"
+      "add.s64 v3, v2, s;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], v1, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], v2, %4, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], v3, %4, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}" ::"r"(d_tmem),
+      "r"(p_tmem), "l"(vdesc), "r"(blk16), "r"(idesc), "r"(acc0), "r"(p_tmem + 8), "r"(p_tmem + 16),
+      "r"(p_tmem + 24), "r"(bar0), "r"(bar1)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T: A (M x K bf16) read from tensor memory,
 // lane = row, two K elements per 32-bit column
 __device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
