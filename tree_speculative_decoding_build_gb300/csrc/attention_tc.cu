@@ -463,78 +463,84 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
       int js = 0, jp = 0, seg = 0;
       bool ostart0 = false, ostart1 = false;
       uint64_t t0 = 0;
+      // running stage / phase of the next PV and the next S (no divisions)
+      int st_p = 0, st_s = 0;
+      uint32_t ph_p = 0, ph_s = 0;
       for (uint32_t spin = 0;; ++spin) {
         bool progressed = false;
-        if (jp < js) {
-          const uint32_t mt = pend[0];
-          const int m_seg = (int)(mt >> 5);
-          const bool m_first = (mt >> 3) & 1;
-          if (__all_sync(0xffffffffu,
-                         mbar_test_wait(smem_u32(&bars.p_full[jp & 1]), (uint32_t)((jp >> 1) & 1)) &&
-                             (!m_first || m_seg == 0 ||
-                              mbar_test_wait(smem_u32(&bars.o_free), (uint32_t)((m_seg - 1) & 1))))) {
-            tc_fence_after();
-            const int x = jp & 1;
-            const int stage = jp % kStages;
-            const uint32_t nblk = mt & 7;
-            const bool acc_first = (mt >> 4) & 1;
-            const uint32_t ap = tmem + kColP + (uint32_t)x * 32;
-            const uint64_t bv = dv + (uint64_t)((stage * kStageBytes) >> 4);
-            const uint32_t od = tmem + kColO + (uint32_t)x * kD;
-            // 16 keys (one paged block) per instruction: A = P from TMEM (8
-            // columns of bf16 pairs), V block i is [2 d halves][16 keys][64 d],
-            // halves kBlkChunk apart (LBO), 8-key groups 1024 B apart (SBO)
-            if (nblk == 4) {
-              umma_pv4_warp(od, ap, bv, kBlkBytes >> 4, idesc_pv, acc_first ? 0u : 1u,
-                            smem_u32(&bars.pv_done[x]), smem_u32(&bars.kv_empty[stage]));
-            } else {
-              for (uint32_t i = 0; i < nblk; ++i)
-                umma_f16_ta_warp(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
-                                 (i > 0 || !acc_first) ? 1u : 0u);
-              umma_commit_warp(smem_u32(&bars.pv_done[x]));
-              umma_commit_warp(smem_u32(&bars.kv_empty[stage]));
-            }
-#pragma unroll
-            for (int i = 0; i + 1 < kStages; ++i) pend[i] = pend[i + 1];
-            ++jp;
-            progressed = true;
+        // all barrier probes first (independent shared-memory reads), then
+        // one vote per candidate MMA
+        const uint32_t mt = pend[0];
+        const int m_seg = (int)(mt >> 5);
+        const bool need_o = ((mt >> 3) & 1) && m_seg > 0;
+        const bool s_first = cur.valid() && cur.seg_start(lo);
+        const bool t_p = mbar_test_wait(smem_u32(&bars.p_full[jp & 1]), (uint32_t)((jp >> 1) & 1));
+        const bool t_o = mbar_test_wait(smem_u32(&bars.o_free), (uint32_t)((m_seg - 1) & 1));
+        const bool t_f = mbar_test_wait(smem_u32(&bars.s_free[js & 1]), (uint32_t)(((js - 2) >> 1) & 1));
+        const bool t_q = mbar_test_wait(smem_u32(&bars.q_full), (uint32_t)(seg & 1));
+        const bool t_k = mbar_test_wait(smem_u32(&bars.kv_full[st_s]), ph_s);
+        const bool go_pv = __all_sync(0xffffffffu, (jp < js) & t_p & (t_o | !need_o));
+        const bool go_s = __all_sync(0xffffffffu, cur.valid() & (t_f | (js < 2)) & (t_q | !s_first) & t_k);
+        if (go_pv) {
+          tc_fence_after();
+          const int x = jp & 1;
+          const uint32_t nblk = mt & 7;
+          const bool acc_first = (mt >> 4) & 1;
+          const uint32_t ap = tmem + kColP + (uint32_t)x * 32;
+          const uint64_t bv = dv + (uint64_t)((st_p * kStageBytes) >> 4);
+          const uint32_t od = tmem + kColO + (uint32_t)x * kD;
+          // 16 keys (one paged block) per instruction: A = P from TMEM (8
+          // columns of bf16 pairs), V block i is [2 d halves][16 keys][64 d],
+          // halves kBlkChunk apart (LBO), 8-key groups 1024 B apart (SBO)
+          if (nblk == 4) {
+            umma_pv4_warp(od, ap, bv, kBlkBytes >> 4, idesc_pv, acc_first ? 0u : 1u,
+                          smem_u32(&bars.pv_done[x]), smem_u32(&bars.kv_empty[st_p]));
+          } else {
+            for (uint32_t i = 0; i < nblk; ++i)
+              umma_f16_ta_warp(od, ap + 8 * i, bv + i * (kBlkBytes >> 4), idesc_pv,
+                               (i > 0 || !acc_first) ? 1u : 0u);
+            umma_commit_warp(smem_u32(&bars.pv_done[x]));
+            umma_commit_warp(smem_u32(&bars.kv_empty[st_p]));
           }
+#pragma unroll
+          for (int i = 0; i + 1 < kStages; ++i) pend[i] = pend[i + 1];
+          ++jp;
+          if (++st_p == kStages) {
+            st_p = 0;
+            ph_p ^= 1;
+          }
+          progressed = true;
         }
-        if (cur.valid()) {
-          const bool first = cur.seg_start(lo);
-          const int stage = js % kStages;
-          if (__all_sync(0xffffffffu,
-                         (js < 2 || mbar_test_wait(smem_u32(&bars.s_free[js & 1]),
-                                                   (uint32_t)(((js - 2) >> 1) & 1))) &&
-                             (!first || mbar_test_wait(smem_u32(&bars.q_full), (uint32_t)(seg & 1))) &&
-                             mbar_test_wait(smem_u32(&bars.kv_full[stage]),
-                                            (uint32_t)((js / kStages) & 1)))) {
-            tc_fence_after();
-            if (first) {
-              ++seg;
-              ostart0 = ostart1 = false;
-            }
-            const int keys = cur.u == cur.tiles - 1 ? NP : kBN;
-            const uint32_t idesc_s = make_idesc(kM, keys, false);
-            const uint64_t bk = dk + (uint64_t)((stage * kStageBytes) >> 4);
-            const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
-            // A = Q from TMEM (bf16 pairs, 8 columns per 16 dims); K is
-            // [2 d halves][keys][64], 128-byte swizzled
-            umma_s_tile_warp(sc, tmem + kColQ, bk, kKVChunk >> 4, idesc_s, smem_u32(&bars.s_full[js & 1]));
-            if (cur.seg_end()) umma_commit_warp(smem_u32(&bars.q_empty));
-            const bool par = js & 1;
-            const bool acc_first = par ? !ostart1 : !ostart0;
-            if (par) ostart1 = true;
-            else ostart0 = true;
-            const uint32_t mt = (uint32_t)(keys >> 4) | ((uint32_t)first << 3) |
-                                ((uint32_t)acc_first << 4) | ((uint32_t)(seg - 1) << 5);
-#pragma unroll
-            for (int i = 0; i < kStages; ++i)
-              if (i == js - jp) pend[i] = mt;
-            ++js;
-            cur.next();
-            progressed = true;
+        if (go_s) {
+          tc_fence_after();
+          if (s_first) {
+            ++seg;
+            ostart0 = ostart1 = false;
           }
+          const int keys = cur.u == cur.tiles - 1 ? NP : kBN;
+          const uint32_t idesc_s = make_idesc(kM, keys, false);
+          const uint64_t bk = dk + (uint64_t)((st_s * kStageBytes) >> 4);
+          const uint32_t sc = tmem + (uint32_t)(js & 1) * kBN;
+          // A = Q from TMEM (bf16 pairs, 8 columns per 16 dims); K is
+          // [2 d halves][keys][64], 128-byte swizzled
+          umma_s_tile_warp(sc, tmem + kColQ, bk, kKVChunk >> 4, idesc_s, smem_u32(&bars.s_full[js & 1]));
+          if (cur.seg_end()) umma_commit_warp(smem_u32(&bars.q_empty));
+          const bool par = js & 1;
+          const bool acc_first = par ? !ostart1 : !ostart0;
+          if (par) ostart1 = true;
+          else ostart0 = true;
+          const uint32_t nmt = (uint32_t)(keys >> 4) | ((uint32_t)s_first << 3) |
+                               ((uint32_t)acc_first << 4) | ((uint32_t)(seg - 1) << 5);
+#pragma unroll
+          for (int i = 0; i < kStages; ++i)
+            if (i == js - jp) pend[i] = nmt;
+          ++js;
+          if (++st_s == kStages) {
+            st_s = 0;
+            ph_s ^= 1;
+          }
+          cur.next();
+          progressed = true;
         }
         if (!cur.valid() && jp == js) break;
         if (progressed) {
