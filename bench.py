@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default="stress")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiling)")
     return ap.parse_args()
 
 
@@ -185,7 +187,8 @@ def bench_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = workloads.make(args.workload, dev, seed=workloads.get(args.workload).seed + rank)
+    inp = workloads.make(args.workload, dev, seed=workloads.get(args.workload).seed + rank,
+                         B=args.batch)
     step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
                          inp["max_blocks"], window_left=inp["window_left"],
                          logits_dtype=inp["logits_dtype"], device=dev)
