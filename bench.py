@@ -56,6 +56,28 @@ def dist_info():
     return rank, world, local
 
 
+def rank_seed(name, rank):
+    """Each rank verifies its own batch: the workload's seed offset by the rank."""
+    import workloads
+    return workloads.get(name).seed + rank
+
+
+def max_over_ranks(x, world, device):
+    """The largest of every rank's ``x`` (a time), on every rank."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, ms):
+    """Whole-job steps/s: every rank ran ``steps`` steps, the slowest took ``ms``."""
+    return world * steps / (ms * 1e-3)
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -153,15 +175,17 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def workload_config(inp, name):
-    import numpy as np
-    ctx = inp["ctx_len"].cpu().numpy()
+def workload_config(name, B=None):
+    """The workload, described from its specification (both arms use this)."""
+    import workloads
+    w = workloads.get(name)
+    B = w.B if B is None else B
+    ctx = f"{w.ctx[0]}..{w.ctx[1]}" if isinstance(w.ctx, tuple) else str(w.ctx)
     return {
-        "workload": (f"{name}: B={inp['B']} ctx={int(ctx.min())}..{int(ctx.max())} N={inp['N']} "
-                     f"Hq/Hkv/D={inp['Hq']}/{inp['Hkv']}/{inp['D']} bf16 KV, block 16, "
-                     f"V={inp['V']} {inp['logits_dtype']} logits"),
-        "batch": inp["B"], "tree_nodes": inp["N"], "ctx_len": int(np.median(ctx)),
-        "window_left": inp["window_left"],
+        "workload": (f"{name}: B={B} ctx={ctx} N={w.N} Hq/Hkv/D={w.Hq}/{w.Hkv}/{w.D} bf16 KV, "
+                     f"block 16{', shuffled block tables' if w.shuffle_blocks else ''}, "
+                     f"V={w.V} {w.logits_dtype} logits"),
+        "batch": B, "tree_nodes": w.N, "ctx_len": ctx, "window_left": w.window_left,
         "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)",
     }
 
@@ -187,8 +211,7 @@ def bench_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = workloads.make(args.workload, dev, seed=workloads.get(args.workload).seed + rank,
-                         B=args.batch)
+    inp = workloads.make(args.workload, dev, seed=rank_seed(args.workload, rank), B=args.batch)
     step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
                          inp["max_blocks"], window_left=inp["window_left"],
                          logits_dtype=inp["logits_dtype"], device=dev)
@@ -246,10 +269,7 @@ def bench_ours(args, rank, world, local):
     clocks = sampler.stop() if rank == 0 else None
     ms = t0.elapsed_time(t1)
     attn_ms = sum(a.elapsed_time(b) for a, b in attn_ev) / K
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(ms, world, dev)
     status_ok = bool((o.status == 0).all().item())
 
     # end to end through the public API: pinned host inputs in, tokens out
@@ -281,10 +301,7 @@ def bench_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / E
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
         return None
@@ -293,7 +310,7 @@ def bench_ours(args, rank, world, local):
     achieved = alg / (attn_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC,
-        "value": world * K / (ms * 1e-3),
+        "value": job_throughput(world, K, ms),
         "unit": "steps/s",
         "n_gpus": world,
         "steps": K,
@@ -305,22 +322,20 @@ def bench_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "impl": "ours",
-        "config": workload_config(inp, args.workload),
+        "config": workload_config(args.workload, args.batch),
         "attention": {"ms": attn_ms, "kv_gbs": achieved, "algorithmic_bytes": alg,
                       "frac_of_8tbs_nominal": achieved / 8000.0,
                       "frac_of_peak": achieved / peak, "peak_kind": peak_kind},
         "roofline": {"kernel": "tv_tree_attention", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(), "peak_source": peak_kind},
-        "e2e": {"value": world / (e2e_ms * 1e-3), "unit": "steps/s",
+        "e2e": {"value": job_throughput(world, 1, e2e_ms), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
         "status_ok": status_ok,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
-    elif not args.no_cpu_baseline and rank == 0:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
     return line
 
@@ -355,31 +370,78 @@ def cpu_baseline(name, budget_s=12.0, seqs_max=None):
                       f"{spent:.1f} s of oracle time scaled by {B}/{done}"}
 
 
+def oracle_step_sample(npi, heads):
+    """One verify step of the oracle on a one-sequence input, attention limited
+    to the first ``heads`` query heads.  Returns (attention seconds, rest seconds)."""
+    import numpy as np
+    import oracle
+    t0 = time.perf_counter()
+    mask, pos, status = oracle.ancestors(npi["parent"], npi["depth"], npi["ctx_len"])
+    t1 = time.perf_counter()
+    Hq = npi["q"].shape[2]
+    sel = np.zeros((1, Hq), bool)
+    sel[:, :heads] = True
+    oracle.attention(npi["q"], npi["k_tree"], npi["v_tree"], npi["k_cache"], npi["v_cache"],
+                     npi["block_table"], npi["ctx_len"], mask, pos,
+                     window_left=npi["window_left"], row_sel=sel)
+    t2 = time.perf_counter()
+    N = npi["tokens"].shape[1]
+    am = oracle.argmax(npi["logits"].reshape(N, -1), npi["logits_dtype"]).reshape(1, N)
+    _, _, acc_nodes, n_acc = oracle.walk(npi["tokens"], npi["parent"], am, npi["root_pred"],
+                                         status)
+    oracle.commit(npi["k_tree"], npi["v_tree"], acc_nodes, n_acc, npi["ctx_len"],
+                  npi["block_table"], npi["k_cache"], npi["v_cache"])
+    t3 = time.perf_counter()
+    return t2 - t1, (t1 - t0) + (t3 - t2)
+
+
+def reference_plan(est_attn_s, est_rest_s, Hq, steps, warmup, budget_s=150.0):
+    """Query heads of attention per sampled step so that (steps + warmup) steps of
+    one sequence fit in ``budget_s``: all heads when they fit, else fewer."""
+    per_head = est_attn_s / Hq
+    room = budget_s / max(1, steps + warmup) - est_rest_s
+    heads = int(room // per_head) if per_head > 0 else Hq
+    return max(1, min(Hq, heads))
+
+
 def bench_reference(args, rank, world):
+    """The oracle on the host cores: exactly K timed steps after W warm-up steps,
+    each on a bounded sample (one sequence of the workload; all query heads when
+    the run fits in a few minutes, else the first h of them), scaled to a whole
+    batch.  Only rank 0 runs under torchrun."""
     if rank != 0:
         return None
-    K, W = max(1, args.steps), max(0, args.warmup)
-    # each step is a bounded sample: one sequence of the workload, scaled to B
     import workloads
+    import oracle
+    K, W = max(1, args.steps), max(0, args.warmup)
     w = workloads.get(args.workload)
-    # keep the whole run within a few minutes
-    K = min(K, 3)
-    W = min(W, 1)
+    oracle.build()
+    npi = workloads.to_numpy(workloads.make(args.workload, "cpu", seed=w.seed + 7919, B=1))
+    Hq = npi["q"].shape[2]
+    ea, er = oracle_step_sample(npi, Hq)
+    heads = reference_plan(ea, er, Hq, K, W)
     for _ in range(W):
-        cpu_baseline(args.workload, budget_s=0.0, seqs_max=1)
+        oracle_step_sample(npi, heads)
     t = time.perf_counter()
-    vals = [cpu_baseline(args.workload, budget_s=0.0, seqs_max=1) for _ in range(K)]
+    attn_s = rest_s = 0.0
+    for _ in range(K):
+        a, r = oracle_step_sample(npi, heads)
+        attn_s += a
+        rest_s += r
     elapsed = time.perf_counter() - t
-    value = sum(v["value"] for v in vals) / len(vals)
-    cb = dict(vals[-1])
-    cb["value"] = value
-    cb["sample"] = (f"each of {K} steps: 1 of {w.B} sequences of the {args.workload} workload, "
-                    f"full verify step, scaled by {w.B}")
+    # one whole-batch step: B sequences, attention over all Hq heads
+    Bj = w.B if args.batch is None else args.batch
+    per_step = Bj * (attn_s / K * Hq / heads + rest_s / K)
+    value = 1.0 / per_step
+    cb = {"value": value, "unit": "steps/s", "cores": oracle.num_threads(), "kind": "oracle",
+          "sample": (f"each of {K} steps: 1 of {Bj} sequences of the {args.workload} workload, "
+                     f"full verify step with attention over {heads} of {Hq} query heads; "
+                     f"attention time scaled by {Hq}/{heads}, the step by {Bj}")}
     return {
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{args.workload} (oracle on host cores)"},
+        "config": workload_config(args.workload, args.batch),
         "cpu_baseline": cb,
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": elapsed,
