@@ -168,8 +168,9 @@ tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
                             size_t workspace_bytes, tv_stream stream);
 
 /*
- * Bytes of scratch tv_argmax needs for `rows` rows of `V` logits of `dtype`
- * (0 when every row is reduced by one thread block).
+ * Bytes of scratch tv_argmax needs for `rows` rows of `V` logits of `dtype`:
+ * room for the (value, index) partials of rows that are cut between thread
+ * blocks, whichever plan the call takes (0 when no plan cuts a row).
  */
 size_t tv_argmax_workspace_size(int64_t rows, int64_t V, int dtype);
 
@@ -182,8 +183,13 @@ size_t tv_argmax_workspace_size(int64_t rows, int64_t V, int dtype);
  *                             lowest index, +0 == -0, a NaN counts as -inf
  *                             (a row of NaN / -inf only gives 0)
  *   workspace  >= tv_argmax_workspace_size(rows, V, dtype) bytes, 16-aligned
+ * Dense rows (row_stride == V, 16-byte aligned base, V * element size a
+ * multiple of 16) with at least 32 KiB of logits per SM are streamed in equal
+ * contiguous ranges, one per warp of a one-block-per-SM grid; other inputs
+ * take one thread block per row chunk.  Both give the same indices.
  * Errors: TV_ERR_ARG (NULL pointers, V < 1, row_stride < V, rows or V beyond
- * int32 indexing, small workspace), TV_ERR_UNSUPPORTED (other dtypes).
+ * int32 indexing, small workspace), TV_ERR_UNSUPPORTED (other dtypes),
+ * TV_ERR_CUDA (launch failure).
  */
 tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
                     int64_t row_stride, int32_t *out_idx, void *workspace,

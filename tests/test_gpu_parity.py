@@ -78,8 +78,12 @@ def bf16_bits(t):
     return t.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
+# (61, 50000), (3, 2097152), (999, 3000), (1000, 4096) and the two large shapes
+# take the streaming plan (rows cut by warp-range boundaries, many rows per
+# range, one row over hundreds of ranges); the others the chunk plan.
 @pytest.mark.parametrize("rows,V", [(1, 1), (3, 7), (8, 1024), (16, 262144), (2048, 151936),
-                                    (5, 100003), (300, 4099)])
+                                    (5, 100003), (300, 4099), (61, 50000), (3, 2097152),
+                                    (999, 3000), (1000, 4096)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_argmax_matches_oracle(tv, rows, V, dtype):
     g = torch.Generator(device="cuda").manual_seed(rows * 7 + V)
@@ -108,6 +112,52 @@ def test_argmax_special_values(tv):
         idx = torch.empty(5, dtype=torch.int32, device="cuda")
         tv.tv_argmax(t, idx)
         assert list(idx.cpu().numpy()) == [1, 2, 0, 0, 0]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_argmax_special_rows_across_cta_boundaries(tv, dtype):
+    """Streaming plan: each 100000-wide row spans many warp ranges, so ties,
+    -inf and NaN rows are merged across partials."""
+    rows, V = 40, 100000
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn(rows, V, generator=g, device="cuda").to(dtype)
+    inf, nan = float("inf"), float("nan")
+    x[0] = -inf
+    x[1] = nan
+    x[2] = 1.0
+    x[3] = nan
+    x[3, V - 1] = 2.0
+    x[4] = -inf
+    x[4, :10] = nan
+    x[5, V // 5] = 7.0
+    x[5, 4 * V // 5] = 7.0
+    x[6] = 0.0
+    x[6, ::2] = -0.0
+    x[7, ::3] = 9.0
+    idx = torch.empty(rows, dtype=torch.int32, device="cuda")
+    tv.tv_argmax(x, idx)
+    got = idx.cpu().numpy()
+    dt = "bf16" if dtype == torch.bfloat16 else "f32"
+    ref = oracle.argmax(bf16_bits(x) if dt == "bf16" else x.cpu().numpy(), dt)
+    assert list(got[:8]) == [0, 0, 0, V - 1, 0, V // 5, 0, 0]
+    assert np.array_equal(got, ref)
+
+
+def test_argmax_plans_agree(tv):
+    """The same rows through the chunk plan (strided view) and the streaming
+    plan (dense copy) give the same indices."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    base = torch.randn(64, 50008, generator=g, device="cuda").to(torch.bfloat16)
+    base[:, ::89] = 4.0
+    strided = base[:, :50000]
+    dense = strided.contiguous()
+    a = torch.empty(64, dtype=torch.int32, device="cuda")
+    b = torch.empty(64, dtype=torch.int32, device="cuda")
+    tv.tv_argmax(strided, a)
+    tv.tv_argmax(dense, b)
+    assert torch.equal(a, b)
+    assert np.array_equal(b.cpu().numpy(), oracle.argmax(bf16_bits(dense), "bf16"))
+    assert tv.tv_argmax_workspace_size(64, 50000, tv.TV_BF16) > 0
 
 
 def test_argmax_strided_and_unaligned_rows(tv):

@@ -828,40 +828,56 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
 }
 
 // Merge the partials of every (sequence, KV head) pair whose tiles were split
-// across CTAs.  One warp per output row; lane l owns dims 4l .. 4l+3.
-__global__ void attn_tc_combine_kernel(const TcParams tp, int P) {
+// across CTAs.  Blocks (c-1, y) with 1 <= c < P own the pair that CTA c-1
+// started and that runs past CTA c-1's range: the pair holding CTA c-1's last
+// flat tile.  Every split pair has exactly one such c; the other blocks exit
+// after one look at the tile offsets (staged in shared memory).  Block row y
+// takes output rows 8y .. 8y+7, one per warp; lane l owns dims 4l .. 4l+3.
+__global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp, int P) {
   const AttnParams &p = tp.a;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  const long long rows = (long long)p.B * p.Hkv * p.R;
-  if (row >= rows) return;
-  const int pair = (int)(row / p.R), m = (int)(row - (long long)pair * p.R);
-  const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
-  const long long T = tp.pre_out[p.B];
-  const int tiles = (tp.pre_out[b + 1] - tp.pre_out[b]) / p.Hkv;
-  const long long S = tp.pre_out[b] + (long long)kvh * tiles, E = S + tiles;
-  auto cta_of = [&](long long f) { return (int)(((f + 1) * P + T - 1) / T - 1); };
+  __shared__ int s_pre[kMaxB + 1];
+  for (int i = threadIdx.x; i <= p.B; i += blockDim.x) s_pre[i] = tp.pre_out[i];
+  __syncthreads();
+  const int c = blockIdx.x + 1;
+  const int m = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const long long T = s_pre[p.B];
+  const long long loc = (long long)c * T / P;
+  if (loc == 0 || loc >= T || m >= p.R) return;
+  const long long f = loc - 1;  // last tile of CTA c-1 (when that range is non-empty)
+  // sequence b with s_pre[b] <= f < s_pre[b+1]
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_pre[mid] <= f) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int tiles = (s_pre[b + 1] - s_pre[b]) / p.Hkv;
+  const int kvh = (int)((f - s_pre[b]) / tiles);
+  const long long S = s_pre[b] + (long long)kvh * tiles, E = S + tiles;
+  auto cta_of = [&](long long x) { return (int)(((x + 1) * P + T - 1) / T - 1); };
   const int c0 = cta_of(S), c1 = cta_of(E - 1);
-  if (c0 == c1) return;  // written directly by its CTA
-  // CTA c covers flat tiles [c*T/P, (c+1)*T/P); ranges can be empty when T < P
+  if (c0 != c - 1 || c1 == c0) return;
+  const int lane = threadIdx.x & 31;
+  // CTA d covers flat tiles [d*T/P, (d+1)*T/P); ranges can be empty when T < P
   float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c) {
-    const long long loc = (long long)c * T / P;
-    if (loc == (long long)(c + 1) * T / P) continue;
-    const int slot = 2 * c + ((c == c0 && loc < S) ? 1 : 0);
+  for (int d = c0; d <= c1; ++d) {
+    const long long ld = (long long)d * T / P;
+    if (ld == (long long)(d + 1) * T / P) continue;
+    const int slot = 2 * d + ((d == c0 && ld < S) ? 1 : 0);
     M = fmaxf(M, tp.part_ml[(size_t)slot * kM + m].x);
   }
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = c0; c <= c1; ++c) {
-    const long long loc = (long long)c * T / P;
-    if (loc == (long long)(c + 1) * T / P) continue;
-    const int slot = 2 * c + ((c == c0 && loc < S) ? 1 : 0);
+  for (int d = c0; d <= c1; ++d) {
+    const long long ld = (long long)d * T / P;
+    if (ld == (long long)(d + 1) * T / P) continue;
+    const int slot = 2 * d + ((d == c0 && ld < S) ? 1 : 0);
     const float2 ml = tp.part_ml[(size_t)slot * kM + m];
     if (ml.x == -INFINITY) continue;
     const float w = exp2f(ml.x - M);
     L += ml.y * w;
-    const float4 o = *reinterpret_cast<const float4 *>(tp.part_o + ((size_t)slot * kM + m) * kD + lane * 4);
+    const float4 o =
+        *reinterpret_cast<const float4 *>(tp.part_o + ((size_t)slot * kM + m) * kD + lane * 4);
     acc.x += o.x * w;
     acc.y += o.y * w;
     acc.z += o.z * w;
@@ -967,9 +983,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   attn_tc_kernel<<<P, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long rows = (long long)a.B * a.Hkv * a.R;
-  const int wpb = 8;
-  attn_tc_combine_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, stream>>>(tp, P);
+  if (P > 1) attn_tc_combine_kernel<<<dim3(P - 1, (a.R + 7) / 8), 256, 0, stream>>>(tp, P);
   return cudaGetLastError();
 }
 
