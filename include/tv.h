@@ -205,12 +205,13 @@ tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
  * device) is not allowed.  Such callers cannot provide tv_argmax's workspace.
  *
  * Same arguments, result and errors as tv_argmax, minus the workspace.  The
- * split partials live in one fixed array of 8192 (value, index) pairs (64 KiB)
- * in the library's static device memory, which every GPU that loads the
- * library keeps until the process exits.  A shape whose plan needs more pairs
- * than that returns TV_ERR_SCRATCH_LIMIT and launches nothing (on a 152-SM GPU
- * no shape needs more than about 2,500).  The call allocates nothing: no
- * cudaMalloc, no cudaFree, no allocating library routine.
+ * split partials live in one fixed array of 8192 (value, index) pairs
+ * (64 KiB) in the library's static device memory, which every GPU that loads
+ * the library keeps until the process exits.  A shape whose plan needs more
+ * pairs than that returns TV_ERR_SCRATCH_LIMIT and launches nothing (on a
+ * 152-SM GPU no shape needs more than 4,864: two per warp of the streaming
+ * plan).  The call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
  *
  * The first call made with a given device current looks up the array's device
  * address (cudaGetSymbolAddress) and caches it; make that first call before

@@ -266,6 +266,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   const long long hi = (long long)(blockIdx.x + 1) * T / P;
   if (blockIdx.x == 0)
     for (int b = tid; b <= B; b += kThreads) tp.pre_out[b] = s_pre[b];
+  // Let the combine grid be scheduled as CTAs of this grid exit; it waits for
+  // this grid's completion (and memory) before it reads anything.
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   volatile int *abort_flag = &s_abort;
 
   Cursor cur{s_pre, B, Hkv, hi, hi, 0, 0, 0, 1};
@@ -832,17 +835,21 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
 // started and that runs past CTA c-1's range: the pair holding CTA c-1's last
 // flat tile.  Every split pair has exactly one such c; the other blocks exit
 // after one look at the tile offsets (staged in shared memory).  Block row y
-// takes output rows 8y .. 8y+7, one per warp; lane l owns dims 4l .. 4l+3.
-__global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp, int P) {
+// takes output rows 32y .. 32y+31, four per warp (their loads issued
+// together); lane l owns dims 4l .. 4l+3.  Launched as a programmatic
+// dependent of the attention grid: it waits for that grid before any read.
+constexpr int kCombRows = 4;  // rows per warp
+__global__ void __launch_bounds__(256, 4) attn_tc_combine_kernel(const TcParams tp, int P) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const AttnParams &p = tp.a;
   __shared__ int s_pre[kMaxB + 1];
   for (int i = threadIdx.x; i <= p.B; i += blockDim.x) s_pre[i] = tp.pre_out[i];
   __syncthreads();
   const int c = blockIdx.x + 1;
-  const int m = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int m0 = blockIdx.y * (8 * kCombRows) + (threadIdx.x >> 5) * kCombRows;
   const long long T = s_pre[p.B];
   const long long loc = (long long)c * T / P;
-  if (loc == 0 || loc >= T || m >= p.R) return;
+  if (loc == 0 || loc >= T || m0 >= p.R) return;
   const long long f = loc - 1;  // last tile of CTA c-1 (when that range is non-empty)
   // sequence b with s_pre[b] <= f < s_pre[b+1]
   int lo = 0, hi = p.B - 1;
@@ -859,37 +866,63 @@ __global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp,
   if (c0 != c - 1 || c1 == c0) return;
   const int lane = threadIdx.x & 31;
   // CTA d covers flat tiles [d*T/P, (d+1)*T/P); ranges can be empty when T < P
-  float M = -INFINITY;
-  for (int d = c0; d <= c1; ++d) {
+  auto slot_of = [&](int d) {
     const long long ld = (long long)d * T / P;
-    if (ld == (long long)(d + 1) * T / P) continue;
-    const int slot = 2 * d + ((d == c0 && ld < S) ? 1 : 0);
-    M = fmaxf(M, tp.part_ml[(size_t)slot * kM + m].x);
-  }
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ld == (long long)(d + 1) * T / P) return -1;
+    return 2 * d + ((d == c0 && ld < S) ? 1 : 0);
+  };
+  float M[kCombRows];
+#pragma unroll
+  for (int i = 0; i < kCombRows; ++i) M[i] = -INFINITY;
   for (int d = c0; d <= c1; ++d) {
-    const long long ld = (long long)d * T / P;
-    if (ld == (long long)(d + 1) * T / P) continue;
-    const int slot = 2 * d + ((d == c0 && ld < S) ? 1 : 0);
-    const float2 ml = tp.part_ml[(size_t)slot * kM + m];
-    if (ml.x == -INFINITY) continue;
-    const float w = exp2f(ml.x - M);
-    L += ml.y * w;
-    const float4 o =
-        *reinterpret_cast<const float4 *>(tp.part_o + ((size_t)slot * kM + m) * kD + lane * 4);
-    acc.x += o.x * w;
-    acc.y += o.y * w;
-    acc.z += o.z * w;
-    acc.w += o.w * w;
+    const int slot = slot_of(d);
+    if (slot < 0) continue;
+#pragma unroll
+    for (int i = 0; i < kCombRows; ++i)
+      if (m0 + i < p.R) M[i] = fmaxf(M[i], tp.part_ml[(size_t)slot * kM + m0 + i].x);
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int t = m / p.G, g = m - t * p.G;
-  __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * kD + lane * 4;
-  uint2 w;
-  w.x = pack_bf16(acc.x * inv, acc.y * inv);
-  w.y = pack_bf16(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2 *>(dst) = w;
+  float L[kCombRows];
+  float4 acc[kCombRows];
+#pragma unroll
+  for (int i = 0; i < kCombRows; ++i) {
+    L[i] = 0.f;
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int d = c0; d <= c1; ++d) {
+    const int slot = slot_of(d);
+    if (slot < 0) continue;
+    float2 ml[kCombRows];
+    float4 o[kCombRows];
+#pragma unroll
+    for (int i = 0; i < kCombRows; ++i) {
+      if (m0 + i < p.R) {
+        ml[i] = tp.part_ml[(size_t)slot * kM + m0 + i];
+        o[i] = *reinterpret_cast<const float4 *>(tp.part_o + ((size_t)slot * kM + m0 + i) * kD + lane * 4);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kCombRows; ++i) {
+      if (m0 + i >= p.R || ml[i].x == -INFINITY) continue;
+      const float w = exp2f(ml[i].x - M[i]);
+      L[i] += ml[i].y * w;
+      acc[i].x += o[i].x * w;
+      acc[i].y += o[i].y * w;
+      acc[i].z += o[i].z * w;
+      acc[i].w += o[i].w * w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kCombRows; ++i) {
+    const int m = m0 + i;
+    if (m >= p.R) break;
+    const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
+    const int t = m / p.G, g = m - t * p.G;
+    __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * kD + lane * 4;
+    uint2 w;
+    w.x = pack_bf16(acc[i].x * inv, acc[i].y * inv);
+    w.y = pack_bf16(acc[i].z * inv, acc[i].w * inv);
+    *reinterpret_cast<uint2 *>(dst) = w;
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -983,7 +1016,20 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   attn_tc_kernel<<<P, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (P > 1) attn_tc_combine_kernel<<<dim3(P - 1, (a.R + 7) / 8), 256, 0, stream>>>(tp, P);
+  if (P > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P - 1, (a.R + 8 * kCombRows - 1) / (8 * kCombRows));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_tc_combine_kernel, tp, (int)P);
+    if (e != cudaSuccess) return e;
+  }
   return cudaGetLastError();
 }
 
