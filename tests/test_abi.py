@@ -1,14 +1,15 @@
 """The C ABI without a GPU: the library builds, loads, exports every function
-that include/tv.h declares, and rejects bad arguments on the host before any
-launch."""
+that the headers under include/ declare, and rejects bad arguments on the host
+before any launch."""
 import ctypes
+import glob
 import os
 import re
 
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "tv.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -19,9 +20,11 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(tv_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(tv_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_step(lib):
@@ -35,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert names
     for f in names:
-        assert hasattr(lib, f), f"{f} declared in tv.h but not exported"
+        assert hasattr(lib, f), f"{f} declared in include/ but not exported"
 
 
 def test_binding_lists_every_export():
@@ -86,3 +89,26 @@ def test_attention_argument_checks(lib):
     assert lib.tv_tree_attention(ctypes.byref(a), None, 0, None) == 1
     a.N, a.B = 8, 0
     assert lib.tv_tree_attention(ctypes.byref(a), None, 0, None) == 0          # nothing to do
+
+
+def test_draft_host_argument_checks(lib):
+    P, I, L, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.tv_topk.argtypes = [P, I, L, L, L, I, P, P, P, S, P]
+    lib.tv_topk.restype = I
+    assert lib.tv_topk(None, 7, 1, 8, 8, 2, None, None, None, 0, None) == 5   # dtype
+    assert lib.tv_topk(None, 0, 1, 8, 8, 0, None, None, None, 0, None) == 1   # k < 1
+    assert lib.tv_topk(None, 0, 1, 8, 8, 9, None, None, None, 0, None) == 1   # k > V
+    assert lib.tv_topk(None, 0, 1, 64, 64, 17, None, None, None, 0, None) == 1  # k > 16
+    assert lib.tv_topk(None, 0, 1, 8, 4, 2, None, None, None, 0, None) == 1   # stride < V
+    assert lib.tv_topk(None, 0, 0, 8, 8, 2, None, None, None, 0, None) == 0   # no rows
+    lib.tv_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
+    lib.tv_build_tree.restype = I
+    args = [None] * 6
+    assert lib.tv_build_tree(None, None, 2, 5, 10, 65, 1, *args) == 1  # budget > 64
+    assert lib.tv_build_tree(None, None, 2, 5, 10, 32, 0, *args) == 1  # w < 1
+    assert lib.tv_build_tree(None, None, 2, 0, 10, 32, 1, *args) == 1  # L < 1
+    assert lib.tv_build_tree(None, None, 2, 5, 10, 32, 1, *args) == 1  # NULL pointers
+    assert lib.tv_build_tree(None, None, 0, 5, 10, 32, 1, *args) == 0  # empty batch
+    lib.tv_topk_workspace_size.argtypes = [L, L, I, I]
+    lib.tv_topk_workspace_size.restype = S
+    assert lib.tv_topk_workspace_size(1, 8, 0, 0) == 0

@@ -7,6 +7,11 @@ bound here through ctypes with the same names:
 
 ``VerifyStep`` owns the output and scratch buffers of one batch shape and
 enqueues the five calls on one CUDA stream with no host synchronisation.
+
+The draft side (``include/tv_draft.h``) builds the tree the step verifies:
+``tv_topk`` gives each draft position's candidate list and ``tv_build_tree``
+expands them best-first into tokens / parent / depth.  ``DraftTree`` owns the
+buffers of one shape and enqueues both calls.
 """
 from __future__ import annotations
 
@@ -15,9 +20,10 @@ import dataclasses
 import torch
 
 from ._lib import (  # noqa: F401
-    BLOCK_SIZE, EXPORTS, LIB_PATH, TV_BF16, TV_ERR_ARG, TV_ERR_BLOCK, TV_ERR_CUDA,
-    TV_ERR_SCRATCH_LIMIT, TV_ERR_TREE, TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError, status_string,
-    tv_argmax, tv_argmax_noalloc, tv_argmax_workspace_size, tv_build_ancestors, tv_commit_kv, tv_tree_attention,
+    BLOCK_SIZE, EXPORTS, LIB_PATH, MAX_NODES, TOPK_MAX, TV_BF16, TV_ERR_ARG, TV_ERR_BLOCK,
+    TV_ERR_CUDA, TV_ERR_SCRATCH_LIMIT, TV_ERR_TREE, TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError,
+    status_string, tv_argmax, tv_argmax_noalloc, tv_argmax_workspace_size, tv_build_ancestors,
+    tv_build_tree, tv_commit_kv, tv_topk, tv_topk_workspace_size, tv_tree_attention,
     tv_tree_attention_workspace_size, tv_tree_walk)
 
 
@@ -80,4 +86,48 @@ class VerifyStep:
         tv_commit_kv(inp["k_tree"], inp["v_tree"], o.acc_nodes, o.n_acc, inp["ctx_len"],
                      inp["block_table"], inp["k_cache"], inp["v_cache"], o.ctx_len_out, o.status,
                      stream)
+        return o
+
+
+@dataclasses.dataclass
+class DraftOutputs:
+    cand_lp: torch.Tensor      # float32 [B, L, K] per-depth candidate log-probs
+    cand_idx: torch.Tensor     # int32 [B, L, K] their token ids
+    tokens: torch.Tensor       # int32 [B, budget]
+    parent: torch.Tensor       # int32 [B, budget]
+    depth: torch.Tensor        # int32 [B, budget]
+    score: torch.Tensor        # float32 [B, budget] cumulative log-prob
+    n_nodes: torch.Tensor      # int32 [B]
+
+
+class DraftTree:
+    """Draft-tree construction for a fixed shape: ``tv_topk`` over the draft
+    log-probabilities [B, L, V] (one row per draft position), then
+    ``tv_build_tree``.  Buffers are allocated once."""
+
+    def __init__(self, B, L, V, K, budget, w=1, dtype=torch.float32, device="cuda"):
+        self.B, self.L, self.V, self.K, self.budget, self.w = B, L, V, K, budget, w
+        dev = torch.device(device)
+        i32, f32 = torch.int32, torch.float32
+        self.out = DraftOutputs(
+            cand_lp=torch.empty(B, L, K, dtype=f32, device=dev),
+            cand_idx=torch.empty(B, L, K, dtype=i32, device=dev),
+            tokens=torch.empty(B, budget, dtype=i32, device=dev),
+            parent=torch.empty(B, budget, dtype=i32, device=dev),
+            depth=torch.empty(B, budget, dtype=i32, device=dev),
+            score=torch.empty(B, budget, dtype=f32, device=dev),
+            n_nodes=torch.empty(B, dtype=i32, device=dev))
+        dt = TV_F32 if dtype == torch.float32 else TV_BF16
+        need = tv_topk_workspace_size(B * L, V, K, dt)
+        self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+
+    def __call__(self, logprobs, stream=None):
+        """``logprobs`` [B, L, V] (float32 or bf16): log-probabilities of each
+        draft position.  Returns the outputs (enqueued on ``stream``)."""
+        o = self.out
+        B, L, V = logprobs.shape
+        tv_topk(logprobs.reshape(B * L, V), self.K, o.cand_lp.view(B * L, self.K),
+                o.cand_idx.view(B * L, self.K), self.ws, stream)
+        tv_build_tree(o.cand_lp, o.cand_idx, self.budget, self.w, o.tokens, o.parent, o.depth,
+                      o.score, o.n_nodes, stream)
         return o

@@ -1,7 +1,7 @@
 """ctypes binding of libtv.so: argument marshalling only.
 
 Each ``tv_*`` function here has the name and argument order of the C entry
-point in ``include/tv.h``; it checks dtypes, devices and contiguity of the
+point in ``include/tv.h`` or ``include/tv_draft.h``; it checks dtypes, devices and contiguity of the
 torch tensors it is given, passes their device pointers, and raises
 ``TvError`` on a non-zero host status.  All arithmetic runs in the library's
 CUDA kernels; there is no fallback of any kind: without the compiled library
@@ -23,6 +23,8 @@ LIB_PATH = _build.LIB
  TV_ERR_SCRATCH_LIMIT) = range(7)
 TV_F32, TV_BF16 = 0, 1
 BLOCK_SIZE = 16
+TOPK_MAX = 16
+MAX_NODES = 64
 
 EXPORTS = (
     "tv_status_string",
@@ -34,6 +36,9 @@ EXPORTS = (
     "tv_argmax_noalloc",
     "tv_tree_walk",
     "tv_commit_kv",
+    "tv_topk_workspace_size",
+    "tv_topk",
+    "tv_build_tree",
 )
 
 
@@ -78,8 +83,12 @@ def _load():
     lib.tv_argmax_noalloc.restype = I
     lib.tv_tree_walk.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]
     lib.tv_commit_kv.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
+    lib.tv_topk_workspace_size.argtypes = [L, L, I, I]
+    lib.tv_topk_workspace_size.restype = S
+    lib.tv_topk.argtypes = [P, I, L, L, L, I, P, P, P, S, P]
+    lib.tv_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
-              "tv_commit_kv"):
+              "tv_commit_kv", "tv_topk", "tv_build_tree"):
         getattr(lib, f).restype = I
     return lib
 
@@ -246,3 +255,39 @@ def tv_commit_kv(k_tree, v_tree, acc_nodes, n_acc, ctx_len_in, block_table, k_ca
         _ptr(block_table, i32, "block_table"), B, N, Hkv, D, block_table.shape[1],
         k_cache.shape[0], _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
         _ptr(ctx_len_out, i32, "ctx_len_out"), _ptr(status, i32, "status"), _stream(stream)))
+
+
+def tv_topk_workspace_size(rows, V, k, dtype):
+    return int(lib.tv_topk_workspace_size(rows, V, k, dtype))
+
+
+def tv_topk(x, k, out_vals, out_idx, workspace=None, stream=None):
+    """The k largest entries of every row of a 2-D ``x`` [rows, V] (rows may be
+    strided) with their indices, in decreasing order."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x: expected a 2-D tensor with unit inner stride")
+    if not x.is_cuda:
+        raise ValueError("x: must be a CUDA tensor")
+    rows, V = x.shape
+    dt = _logits_dtype(x)
+    need = tv_topk_workspace_size(rows, V, k, dt)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    wp = _ptr(workspace, None, "workspace") if workspace is not None else None
+    wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("tv_topk", lib.tv_topk(ctypes.c_void_p(x.data_ptr()), dt, rows, V, x.stride(0), int(k),
+                                  _ptr(out_vals, torch.float32, "out_vals"),
+                                  _ptr(out_idx, torch.int32, "out_idx"), wp, wb, _stream(stream)))
+
+
+def tv_build_tree(cand_lp, cand_idx, budget, w, tokens, parent, depth, score, n_nodes,
+                  stream=None):
+    """Best-first draft tree of ``budget`` nodes from per-depth candidate lists
+    ``cand_lp`` float32 [B, L, K] / ``cand_idx`` int32 [B, L, K]."""
+    B, L, K = cand_lp.shape
+    i32 = torch.int32
+    _check("tv_build_tree", lib.tv_build_tree(
+        _ptr(cand_lp, torch.float32, "cand_lp"), _ptr(cand_idx, i32, "cand_idx"), B, L, K,
+        int(budget), int(w), _ptr(tokens, i32, "tokens"), _ptr(parent, i32, "parent"),
+        _ptr(depth, i32, "depth"), _ptr(score, torch.float32, "score"),
+        _ptr(n_nodes, i32, "n_nodes"), _stream(stream)))

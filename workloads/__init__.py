@@ -447,3 +447,47 @@ def kv_bytes(inp) -> int:
     else:
         vis = ctx
     return int(vis.sum()) * inp["Hkv"] * inp["D"] * 2 * 2
+
+
+# --------------------------------------------------------------------------- draft side
+
+@dataclasses.dataclass(frozen=True)
+class DraftWorkload:
+    """Draft-tree construction inputs: per-position draft log-probabilities."""
+    name: str
+    seed: int
+    B: int        # sequences
+    L: int        # draft positions (maximum tree depth)
+    V: int        # vocabulary
+    K: int        # candidates per position (top_k)
+    budget: int   # tree nodes
+    w: int = 1    # nodes popped per round
+
+
+DRAFT_WORKLOADS = {
+    # DDTree construction (top_k 10, 32-node budget) at the stress batch, depth <= 8
+    "tree_build": DraftWorkload("tree_build", 2000, 64, 8, 151936, 10, 32, 1),
+    # batched top-w rounds of the same shape
+    "tree_build_w4": DraftWorkload("tree_build_w4", 2001, 64, 8, 151936, 10, 32, 4),
+    # leaf-sibling proposer: top-4 per spine position over a 262144-token vocab
+    "top_w": DraftWorkload("top_w", 2002, 1, 4, 262144, 4, 16, 1),
+}
+
+
+def make_draft(name, device="cpu", seed: Optional[int] = None, *, B: Optional[int] = None,
+               L: Optional[int] = None, V: Optional[int] = None, quantum: float = 0.0,
+               dtype=torch.float32):
+    """Draft log-probabilities [B, L, V]: log-softmax of N(0, 1) logits drawn on
+    ``device`` (the drafter's output; the tree construction starts from it).
+    ``quantum`` > 0 rounds the logits to multiples of it first, which makes
+    exactly tied log-probabilities (tests of the tie rules)."""
+    w = DRAFT_WORKLOADS[name]
+    seed = w.seed if seed is None else seed
+    B = w.B if B is None else B
+    L = w.L if L is None else L
+    V = w.V if V is None else V
+    gen = torch.Generator(device=device).manual_seed(seed)
+    logits = torch.randn(B, L, V, generator=gen, device=device, dtype=torch.float32)
+    if quantum > 0:
+        logits = torch.round(logits / quantum) * quantum
+    return torch.log_softmax(logits, dim=-1).to(dtype)
