@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
+    ap.add_argument("--path", choices=["verify", "draft"], default="verify",
+                    help="verify: the verify step (default); draft: draft-tree construction")
+    ap.add_argument("--draft-workload", default="tree_build")
     return ap.parse_args()
 
 
@@ -335,6 +338,11 @@ def bench_ours(args, rank, world, local):
         "status_ok": status_ok,
         "clocks": clocks,
     }
+    if world == 1:
+        # the draft-tree path (the step before verify), timed on its own
+        d = measure_draft("tree_build", 50, 3, dev)
+        d.pop("_inputs")
+        line["draft_path"] = d
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
     return line
@@ -368,6 +376,143 @@ def cpu_baseline(name, budget_s=12.0, seqs_max=None):
             "sample": f"{done} of {B} sequences of the {name} workload, full verify step each "
                       f"(fp64 attention over all heads/nodes, argmax, walk, commit); "
                       f"{spent:.1f} s of oracle time scaled by {B}/{done}"}
+
+
+DRAFT_METRIC = "draft-tree construction steps/s (tv_topk + tv_build_tree) and top-k GB/s"
+
+
+def measure_draft(name, steps, warmup, dev, seed_offset=0, batch=None):
+    """Time the draft path on one GPU: tv_topk over the per-position log-probs,
+    then tv_build_tree; CUDA events on the launching stream around each."""
+    import torch
+    import workloads
+    import tree_speculative_decoding_build_gb300 as tv
+    w = workloads.DRAFT_WORKLOADS[name]
+    B = w.B if batch is None else batch
+    lp = workloads.make_draft(name, dev, seed=w.seed + seed_offset, B=B)
+    dt = tv.DraftTree(B, w.L, w.V, w.K, w.budget, w.w, device=dev)
+    o = dt.out
+    stream = torch.cuda.current_stream(dev)
+    x = lp.view(B * w.L, w.V)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tv.tv_topk(x, w.K, o.cand_lp.view(B * w.L, w.K), o.cand_idx.view(B * w.L, w.K), dt.ws)
+        if ev is not None:
+            ev[1].record(stream)
+        tv.tv_build_tree(o.cand_lp, o.cand_idx, w.budget, w.w, o.tokens, o.parent, o.depth,
+                         o.score, o.n_nodes)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    topk_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    tree_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    topk_bytes = B * w.L * w.V * lp.element_size() + B * w.L * w.K * 8
+    peak, peak_kind = peaks()
+    gbs = topk_bytes / (topk_ms * 1e-3) / 1e9
+    return {
+        "workload": (f"{name}: B={B} L={w.L} V={w.V} fp32 log-probs, top_k={w.K}, "
+                     f"budget={w.budget}, w={w.w}"),
+        "ms_per_step": ms, "steps_per_s": 1000.0 / ms,
+        "tv_topk": {"ms": topk_ms, "bytes": topk_bytes, "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "peak": peak, "peak_source": peak_kind},
+        "tv_build_tree": {"us": tree_ms * 1000.0, "trees": B},
+        "launches_per_step": 3 if tv.tv_topk_workspace_size(B * w.L, w.V, w.K, tv.TV_F32) else 2,
+        "_inputs": (lp, o),
+    }
+
+
+def draft_cpu_baseline(name, budget_s=10.0):
+    """The oracle on a bounded sample of the draft workload: whole sequences
+    (top-k of every position, then the construction) until the budget is spent."""
+    import oracle
+    import workloads
+    from oracle import tree_build as tb
+    w = workloads.DRAFT_WORKLOADS[name]
+    done, spent = 0, 0.0
+    while done < w.B and spent < budget_s:
+        lp = workloads.make_draft(name, "cpu", seed=w.seed + 7919 * (done + 1), B=1).numpy()
+        t = time.perf_counter()
+        vals, idx = tb.topk(lp.reshape(w.L, w.V), w.K, "f32")
+        tb.build_tree(vals.reshape(1, w.L, w.K), idx.reshape(1, w.L, w.K), w.budget, w.w)
+        spent += time.perf_counter() - t
+        done += 1
+    return {"value": 1.0 / (spent / done * w.B), "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.B} sequences of the {name} workload (numpy top-k + "
+                      f"heap construction, one thread), scaled by {w.B}/{done}"}
+
+
+def bench_draft(args, rank, world, local):
+    """--path draft: one JSON line for the draft-tree construction path."""
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    r = measure_draft(args.draft_workload, args.steps, args.warmup, dev, seed_offset=rank,
+                      batch=args.batch)
+    ms = max_over_ranks(r["ms_per_step"], world, dev)
+    lp, o = r.pop("_inputs")
+    # end to end: pinned host log-probs in, trees out
+    lp_host = lp.cpu().pin_memory()
+    outs = [o.tokens, o.parent, o.depth, o.n_nodes]
+    res_host = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    import tree_speculative_decoding_build_gb300 as tv
+    import workloads
+    w = workloads.DRAFT_WORKLOADS[args.draft_workload]
+    B = lp.shape[0]
+    dt = tv.DraftTree(B, w.L, w.V, w.K, w.budget, w.w, device=dev)
+    E = max(1, args.e2e_steps)
+    stream = torch.cuda.current_stream(dev)
+    for it in range(E + 2):
+        if it == 2:
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        lp.copy_(lp_host, non_blocking=True)
+        oo = dt(lp)
+        for h, t in zip(res_host, [oo.tokens, oo.parent, oo.depth, oo.n_nodes]):
+            h.copy_(t, non_blocking=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, world, dev)
+    if rank != 0:
+        return None
+    line = {
+        "metric": DRAFT_METRIC, "value": job_throughput(world, 1, ms), "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "ours", "path": "draft",
+        "config": {"workload": r["workload"], "batch": B,
+                   "l2": "inputs larger than L2 (311 MB of log-probs per step)"},
+        "roofline": {"kernel": "tv_topk", "bound": "hbm", "achieved": r["tv_topk"]["gbs"],
+                     "peak": r["tv_topk"]["peak"], "unit": "GB/s",
+                     "frac": r["tv_topk"]["frac_of_peak"], "traffic": None,
+                     "peak_source": r["tv_topk"]["peak_source"]},
+        "tv_build_tree_us": r["tv_build_tree"]["us"],
+        "e2e": {"value": job_throughput(world, 1, e2e_ms), "unit": "steps/s",
+                "h2d_bytes_per_step": lp_host.numel() * lp_host.element_size(),
+                "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in res_host)},
+        "gpu_launches": r["launches_per_step"] * args.steps,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = draft_cpu_baseline(args.draft_workload)
+    return line
 
 
 def oracle_step_sample(npi, heads):
@@ -461,7 +606,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
-    line = bench_ours(args, rank, world, local)
+    if args.path == "draft":
+        line = bench_draft(args, rank, world, local)
+    else:
+        line = bench_ours(args, rank, world, local)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -38,9 +38,12 @@ def run_topk(tv, x, k):
 
 # ------------------------------------------------------------------ topk
 
+# (16, 262144), (64, 65536), (999, 3000) and (40000, 64) take the streaming
+# plan (rows cut between warp ranges, many rows per load batch); the others the
+# chunk plan.
 @pytest.mark.parametrize("rows,V,k", [(1, 1, 1), (3, 7, 7), (8, 1024, 4), (16, 262144, 4),
                                       (5, 100003, 16), (300, 4099, 10), (1, 40000, 16),
-                                      (64, 65536, 10)])
+                                      (64, 65536, 10), (999, 3000, 10), (40000, 64, 16)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_topk_matches_oracle(tv, rows, V, k, dtype):
     g = torch.Generator(device="cuda").manual_seed(rows * 31 + V + k)
@@ -58,9 +61,10 @@ def test_topk_matches_oracle(tv, rows, V, k, dtype):
     assert np.array_equal(vals, ev)
 
 
+@pytest.mark.parametrize("rows", [8, 40])       # chunk plan, streaming plan
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_topk_special_rows(tv, dtype):
-    rows, V, k = 8, 70000, 16
+def test_topk_special_rows(tv, dtype, rows):
+    V, k = 70000, 16
     g = torch.Generator(device="cuda").manual_seed(3)
     x = torch.randn(rows, V, generator=g, device="cuda").to(dtype)
     inf, nan = float("inf"), float("nan")

@@ -10,25 +10,29 @@
 // the top w candidates per round).
 //
 // tv_topk: one thread block per row chunk (chunks only when there are too few
-// rows to fill the GPU).  Every thread keeps its own sorted list of the 16 best
-// (value, index) pairs it has seen in registers; a 16-byte vector is looked at
-// element by element only when its packed maximum beats the list's last entry.
-// The block then pulls its k best out of the thread lists in k rounds of a
-// block-wide arg-max, and a second kernel merges the chunk lists of a row the
-// same way.  Order: larger value first, equal values lower index first, NaN as
-// -inf; an empty list slot is (-inf, INT32_MAX), which every real element of
-// the row beats, so rows with fewer than k finite values still list real
-// indices.
+// rows to fill the GPU); each of its warps scans a contiguous eighth of the
+// chunk and keeps a sorted list of its 32 best (value, index) pairs spread over
+// its lanes.  A lane's 16-byte vector is looked at element by element only
+// when its packed maximum beats the list's k-th entry; a ballot hands such
+// vectors to the whole warp, which inserts the winning elements with shuffles.
+// After the first few hundred elements almost no vector passes, so the scan
+// runs at memory speed.  Warp 0 then folds the other warps' lists into its
+// own, and a one-warp-per-row kernel folds the chunk lists of a row.  Order:
+// larger value first, equal values lower index first, NaN as -inf; an empty
+// slot is (-inf, INT32_MAX), which every real element of the row beats, so
+// rows with fewer than k finite values still list real indices.
 //
-// tv_build_tree: one warp per sequence, all state in shared memory.  The
-// candidate heap of the construction holds, for every expanded node, all K of
-// its children; since each node's children come in non-increasing score order
-// with increasing push counters, the best candidate among one node's children
-// is always the first one not yet popped.  So the heap is kept as one cursor
-// per expanded node (plus one for the roots), and a pop is a warp-wide arg-max
-// over the cursors' current candidates (higher score, then lower push
-// counter).  Scores are float32 sums added in depth order (__fadd_rn), the
-// same additions the construction defines, so the tree is exact.
+// tv_build_tree: one warp per sequence.  The candidate heap of the
+// construction holds, for every expanded node, all K of its children; since
+// each node's children come in non-increasing score order with increasing push
+// counters, the best candidate among one node's children is always the first
+// one not yet popped.  So the heap is kept as one cursor per expanded node
+// (plus one for the roots), spread over the lanes with each cursor's current
+// candidate in registers, and a pop is a warp-wide arg-max: one redux.max over
+// an order-preserving key of the score, one redux.min over the push counters
+// of the lanes that hold that score.  Scores are float32 sums added in depth
+// order (__fadd_rn), the same additions the construction defines, so the tree
+// is exact.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -39,111 +43,39 @@ namespace tv {
 
 namespace {
 
-constexpr int kTopThreads = 256;
-constexpr int kTopList = TV_TOPK_MAX;  // entries per thread list
-constexpr int kTopUnroll = 4;          // 16-byte loads in flight per thread
+constexpr int kTopWarps = 8;
+constexpr int kTopThreads = 32 * kTopWarps;
+constexpr int kTopUnroll = 4;  // 16-byte loads in flight per lane
 
 // a beats b: larger value, or equal value and lower index
 __device__ __forceinline__ bool beats(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && ai < bi);
 }
 
-struct TopList {
-  float v[kTopList];
-  int i[kTopList];
-
-  __device__ __forceinline__ void init() {
-#pragma unroll
-    for (int j = 0; j < kTopList; ++j) {
-      v[j] = -INFINITY;
-      i[j] = INT32_MAX;
-    }
+// A warp's sorted list of its 32 best (value, index) pairs, lane j holding the
+// j-th; an empty slot is (-inf, INT32_MAX).  Insertion is warp-wide: x / xi
+// must be the same in every lane.
+__device__ __forceinline__ void wl_insert(float &lv, int &li, float x, int xi) {
+  const bool gt = beats(x, xi, lv, li);
+  const unsigned m = __ballot_sync(0xffffffffu, gt);
+  if (m == 0) return;
+  const int p = __ffs(m) - 1;  // the list is sorted: every lane from p on is beaten
+  const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+  const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+  const int lane = threadIdx.x & 31;
+  if (lane > p) {
+    lv = uv;
+    li = ui;
+  } else if (lane == p) {
+    lv = x;
+    li = xi;
   }
-  // insert (x, xi) in order; NaN is -inf
-  __device__ __forceinline__ void push(float x, int xi) {
-    x = (x != x) ? -INFINITY : x;
-    if (!beats(x, xi, v[kTopList - 1], i[kTopList - 1])) return;
-    bool moved = false;
-#pragma unroll
-    for (int j = 0; j < kTopList; ++j) {
-      const bool take = moved || beats(x, xi, v[j], i[j]);
-      if (take) {
-        const float tv = v[j];
-        const int ti = i[j];
-        v[j] = x;
-        i[j] = xi;
-        x = tv;
-        xi = ti;
-      }
-      moved = take;
-    }
-  }
-  // drop the head (after it won a round)
-  __device__ __forceinline__ void pop_head() {
-#pragma unroll
-    for (int j = 0; j < kTopList - 1; ++j) {
-      v[j] = v[j + 1];
-      i[j] = i[j + 1];
-    }
-    v[kTopList - 1] = -INFINITY;
-    i[kTopList - 1] = INT32_MAX;
-  }
-  // smallest entry that still matters: a candidate must beat it
-  __device__ __forceinline__ bool full_above(float m) const {
-    return !(m > v[kTopList - 1]) && i[kTopList - 1] != INT32_MAX;
-  }
-};
-
-// One block-wide arg-max round over the thread lists' heads; every thread gets
-// the winner.  Two barriers per round (kTopThreads threads).
-__device__ __forceinline__ void block_best(const TopList &l, float &wv, int &wi) {
-  __shared__ float sv[kTopThreads / 32];
-  __shared__ int si[kTopThreads / 32];
-  __shared__ float bv;
-  __shared__ int bi;
-  float v = l.v[0];
-  int i = l.i[0];
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (beats(ov, oi, v, i)) {
-      v = ov;
-      i = oi;
-    }
-  }
-  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) {
-    sv[w] = v;
-    si[w] = i;
-  }
-  __syncthreads();
-  if (w == 0) {
-    v = lane < kTopThreads / 32 ? sv[lane] : -INFINITY;
-    i = lane < kTopThreads / 32 ? si[lane] : INT32_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-      if (beats(ov, oi, v, i)) {
-        v = ov;
-        i = oi;
-      }
-    }
-    if (lane == 0) {
-      bv = v;
-      bi = i;
-    }
-  }
-  __syncthreads();
-  wv = bv;
-  wi = bi;
-  __syncthreads();  // bv / bi are rewritten by the next round
 }
 
 __device__ __forceinline__ float elem(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float elem(const float *p) { return *p; }
 
+// Packed maximum of a 16-byte vector (a NaN operand is ignored).
 template <typename T>
 __device__ __forceinline__ float vec_max(const uint4 &w);
 template <>
@@ -160,24 +92,78 @@ __device__ __forceinline__ float vec_max<float>(const uint4 &w) {
                fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
 }
 
+// Element e of a 16-byte vector.
 template <typename T>
-__device__ __forceinline__ void push_vec(TopList &l, const uint4 &w, int i0);
+__device__ __forceinline__ float vec_elem(const uint4 &w, int e);
 template <>
-__device__ __forceinline__ void push_vec<__nv_bfloat16>(TopList &l, const uint4 &w, int i0) {
-  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int k = 0; k < 8; ++k) l.push((k & 1) ? bf16_hi(ws[k >> 1]) : bf16_lo(ws[k >> 1]), i0 + k);
+__device__ __forceinline__ float vec_elem<__nv_bfloat16>(const uint4 &w, int e) {
+  const uint32_t h = (e >> 1) == 0 ? w.x : (e >> 1) == 1 ? w.y : (e >> 1) == 2 ? w.z : w.w;
+  return (e & 1) ? bf16_hi(h) : bf16_lo(h);
 }
 template <>
-__device__ __forceinline__ void push_vec<float>(TopList &l, const uint4 &w, int i0) {
-  l.push(__uint_as_float(w.x), i0);
-  l.push(__uint_as_float(w.y), i0 + 1);
-  l.push(__uint_as_float(w.z), i0 + 2);
-  l.push(__uint_as_float(w.w), i0 + 3);
+__device__ __forceinline__ float vec_elem<float>(const uint4 &w, int e) {
+  return __uint_as_float(e == 0 ? w.x : e == 1 ? w.y : e == 2 ? w.z : w.w);
 }
 
-// grid.x = rows * chunks.  Writes the chunk's k best, in order, to
-// (out_v, out_i) + blockIdx.x * k: the final answer when chunks == 1.
+// Order-preserving int key of a non-NaN float (for a block-wide atomicMax).
+__device__ __forceinline__ int fkey(float f) {
+  const int b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float fkey_inv(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+
+// Lanes flagged in `ballot` hand their vector to the whole warp, one lane at a
+// time in lane order, and its elements that beat the k-th entry go in.
+template <typename T>
+__device__ __forceinline__ void take_flagged(unsigned ballot, const uint4 &q, int idx0, int k,
+                                             float &lv, int &li, float &tv, int &ti) {
+  constexpr int E = 16 / sizeof(T);
+  while (ballot) {
+    const int src = __ffs(ballot) - 1;
+    ballot &= ballot - 1;
+    uint4 w;
+    w.x = __shfl_sync(0xffffffffu, q.x, src);
+    w.y = __shfl_sync(0xffffffffu, q.y, src);
+    w.z = __shfl_sync(0xffffffffu, q.z, src);
+    w.w = __shfl_sync(0xffffffffu, q.w, src);
+    const int i0 = __shfl_sync(0xffffffffu, idx0, src);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float x = vec_elem<T>(w, e);
+      x = (x != x) ? -INFINITY : x;
+      if (beats(x, i0 + e, tv, ti)) {
+        wl_insert(lv, li, x, i0 + e);
+        tv = __shfl_sync(0xffffffffu, lv, k - 1);
+        ti = __shfl_sync(0xffffffffu, li, k - 1);
+      }
+    }
+  }
+}
+
+// The warp's list at the end of a block: warp 0 folds the other warps' k best
+// into its own and returns the block's k best in its lanes 0 .. k-1.
+__device__ __forceinline__ void block_fold(float &lv, int &li, int k) {
+  __shared__ float sv[kTopWarps][32];
+  __shared__ int si[kTopWarps][32];
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  sv[w][lane] = lv;
+  si[w][lane] = li;
+  __syncthreads();
+  if (w == 0) {
+    for (int o = 1; o < kTopWarps; ++o)
+      for (int j = 0; j < k; ++j) {
+        const float x = sv[o][j];
+        const int xi = si[o][j];
+        if (xi == INT32_MAX) break;  // the rest of that list is empty
+        wl_insert(lv, li, x, xi);
+      }
+  }
+}
+
+// grid.x = rows * chunks; warp w of a block scans the w-th eighth of the
+// chunk, so each warp sees its indices in increasing order.  Writes the
+// chunk's k best to (out_v, out_i) + blockIdx.x * k: the final answer when
+// chunks == 1.
 template <typename T>
 __global__ void __launch_bounds__(kTopThreads)
 topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chunks, int chunk_len,
@@ -188,68 +174,282 @@ topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chun
   const int begin = c * chunk_len;
   const int end = min(V, begin + chunk_len);
   const T *xr = x + row * row_stride;
-  TopList l;
-  l.init();
-  int tail = begin;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float lv = -INFINITY, tv = -INFINITY;
+  int li = INT32_MAX, ti = INT32_MAX;  // (tv, ti): the k-th entry, the bar to beat
+  // The block's bar: the largest k-th entry of any warp whose list holds k real
+  // entries.  No value below it can be among the chunk's k best (that warp
+  // already has k values at least as large), so every warp may skip such values.
+  __shared__ int s_bar;
+  if (threadIdx.x == 0) s_bar = fkey(-INFINITY);
+  __syncthreads();
   if (vec) {
+    // items are 16-byte vectors; the warp's share is a contiguous run of them
     const int nvec = (end - begin) / E;
+    const int w0 = (int)((long long)nvec * w / kTopWarps);
+    const int w1 = (int)((long long)nvec * (w + 1) / kTopWarps);
     const uint4 *xv = reinterpret_cast<const uint4 *>(xr + begin);
-    for (int j0 = threadIdx.x; j0 < nvec; j0 += kTopThreads * kTopUnroll) {
-      uint4 w[kTopUnroll];
+    for (int b0 = w0; b0 < w1; b0 += 32 * kTopUnroll) {
+      uint4 q[kTopUnroll];
 #pragma unroll
       for (int u = 0; u < kTopUnroll; ++u) {
-        const int j = j0 + u * kTopThreads;
-        if (j < nvec) w[u] = __ldcs(xv + j);
+        const int j = b0 + lane + 32 * u;
+        if (j < w1) q[u] = __ldcs(xv + j);
       }
+      const float bar = fkey_inv(*(volatile int *)&s_bar);
 #pragma unroll
       for (int u = 0; u < kTopUnroll; ++u) {
-        const int j = j0 + u * kTopThreads;
-        if (j < nvec && !l.full_above(vec_max<T>(w[u]))) push_vec<T>(l, w[u], begin + j * E);
+        const int j = b0 + lane + 32 * u;
+        const float m = vec_max<T>(q[u]);
+        const bool flag = j < w1 && (m > tv || ti == INT32_MAX) && !(m < bar);
+        const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+        if (ballot) take_flagged<T>(ballot, q[u], begin + j * E, k, lv, li, tv, ti);
+      }
+      if (lane == 0 && ti != INT32_MAX) atomicMax(&s_bar, fkey(tv));
+    }
+    // the tail that does not fill a vector: warp 0, one element per lane
+    if (w == 0) {
+      for (int t0 = begin + nvec * E; t0 < end; t0 += 32) {
+        const int i = t0 + lane;
+        float xv1 = i < end ? elem(xr + i) : -INFINITY;
+        xv1 = (xv1 != xv1) ? -INFINITY : xv1;
+        const bool flag = i < end && beats(xv1, i, tv, ti);
+        unsigned ballot = __ballot_sync(0xffffffffu, flag);
+        while (ballot) {
+          const int src = __ffs(ballot) - 1;
+          ballot &= ballot - 1;
+          const float y = __shfl_sync(0xffffffffu, xv1, src);
+          const int yi = __shfl_sync(0xffffffffu, i, src);
+          if (beats(y, yi, tv, ti)) {
+            wl_insert(lv, li, y, yi);
+            tv = __shfl_sync(0xffffffffu, lv, k - 1);
+            ti = __shfl_sync(0xffffffffu, li, k - 1);
+          }
+        }
       }
     }
-    tail = begin + nvec * E;
+  } else {
+    // unaligned rows: one element per lane per step, contiguous run per warp
+    const int n = end - begin;
+    const int w0 = begin + (int)((long long)n * w / kTopWarps);
+    const int w1 = begin + (int)((long long)n * (w + 1) / kTopWarps);
+    for (int t0 = w0; t0 < w1; t0 += 32) {
+      const int i = t0 + lane;
+      float xv1 = i < w1 ? elem(xr + i) : -INFINITY;
+      xv1 = (xv1 != xv1) ? -INFINITY : xv1;
+      const bool flag = i < w1 && beats(xv1, i, tv, ti);
+      unsigned ballot = __ballot_sync(0xffffffffu, flag);
+      while (ballot) {
+        const int src = __ffs(ballot) - 1;
+        ballot &= ballot - 1;
+        const float y = __shfl_sync(0xffffffffu, xv1, src);
+        const int yi = __shfl_sync(0xffffffffu, i, src);
+        if (beats(y, yi, tv, ti)) {
+          wl_insert(lv, li, y, yi);
+          tv = __shfl_sync(0xffffffffu, lv, k - 1);
+          ti = __shfl_sync(0xffffffffu, li, k - 1);
+        }
+      }
+    }
   }
-  for (int i = tail + threadIdx.x; i < end; i += kTopThreads) l.push(elem(xr + i), i);
-  for (int r = 0; r < k; ++r) {
-    float wv;
-    int wi;
-    block_best(l, wv, wi);
-    if (l.i[0] == wi && wi != INT32_MAX) l.pop_head();
-    if (threadIdx.x == 0) {
-      out_v[(size_t)blockIdx.x * k + r] = wv;
-      out_i[(size_t)blockIdx.x * k + r] = wi;
-    }
+  block_fold(lv, li, k);
+  if (w == 0 && lane < k) {
+    out_v[(size_t)blockIdx.x * k + lane] = lv;
+    out_i[(size_t)blockIdx.x * k + lane] = li;
   }
 }
 
-// One block per row: merge the row's chunks * k candidates.
-__global__ void __launch_bounds__(kTopThreads)
-topk_merge_kernel(const float *__restrict__ part_v, const int32_t *__restrict__ part_i, int chunks,
-                  int k, float *__restrict__ out_v, int32_t *__restrict__ out_i) {
-  const long long row = blockIdx.x;
+// One warp per row: fold the row's chunks * k candidates into one list.
+__global__ void topk_merge_kernel(const float *__restrict__ part_v, const int32_t *__restrict__ part_i,
+                                  long long rows, int chunks, int k, float *__restrict__ out_v,
+                                  int32_t *__restrict__ out_i) {
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
   const int n = chunks * k;
-  TopList l;
-  l.init();
-  for (int j = threadIdx.x; j < n; j += kTopThreads)
-    l.push(part_v[row * n + j], part_i[row * n + j]);
-  for (int r = 0; r < k; ++r) {
-    float wv;
-    int wi;
-    block_best(l, wv, wi);
-    if (l.i[0] == wi && wi != INT32_MAX) l.pop_head();
-    if (threadIdx.x == 0) {
-      out_v[row * k + r] = wv;
-      out_i[row * k + r] = wi;
-    }
+  float lv = -INFINITY;
+  int li = INT32_MAX;
+  for (int j = 0; j < n; ++j) {
+    const int xi = part_i[row * n + j];
+    if (xi == INT32_MAX) continue;
+    wl_insert(lv, li, part_v[row * n + j], xi);
+  }
+  if (lane < k) {
+    out_v[row * k + lane] = lv;
+    out_i[row * k + lane] = li;
   }
 }
+
+// Order-preserving unsigned key of a non-NaN float; 0 is below every float.
+__device__ __forceinline__ unsigned score_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float score_unkey(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ------------------------------------------------------------------ stream plan
+//
+// Dense, aligned rows: the flattened [rows x V] array is cut into equal
+// contiguous ranges, one per warp of a one-CTA-per-SM grid (the argmax stream
+// plan with a k-list instead of one pair), so every SM moves the same bytes
+// and there is no tail wave.  A warp's list covers the piece of the current
+// row inside its range; at a row end the list is written (a row lying whole in
+// the range goes straight to the output, the range's first and last pieces to
+// slots 2w and 2w+1), and a merge kernel folds the pieces of the rows cut by
+// range boundaries.
+
+constexpr int kTsWarps = 16;   // warps per CTA
+constexpr int kTsUnroll = 8;   // 16-byte loads per lane per batch (two batches in flight)
+
+__device__ __forceinline__ long long ts_split(long long w, long long nv, long long owners) {
+  return w * nv / owners;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kTsWarps, 1)
+topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long long owners, int k,
+                   float *__restrict__ part_v, int32_t *__restrict__ part_i,
+                   float *__restrict__ out_v, int32_t *__restrict__ out_i) {
+  constexpr int E = 16 / sizeof(T);
+  constexpr int kBatch = 32 * kTsUnroll;
+  const int lane = threadIdx.x & 31;
+  const long long w = (long long)blockIdx.x * kTsWarps + (threadIdx.x >> 5);
+  if (w >= owners) return;
+  const long long v0 = ts_split(w, nv, owners), v1 = ts_split(w + 1, nv, owners);
+  const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+  long long r = v0 / vpr, rs = r * vpr;
+  float lv = -INFINITY, tv = -INFINITY;
+  int li = INT32_MAX, ti = INT32_MAX;
+  // bar: a lower bound of the current row piece's k-th largest value; values
+  // below it cannot be in the piece's k best and are skipped unexamined
+  float bar = -INFINITY;
+  bool fresh = true;  // nothing of the current row piece seen yet
+
+  // close the piece of row r that ends at vector pe
+  auto emit = [&](long long pe) {
+    const long long ps = max(rs, v0);
+    if (lane < k) {
+      if (ps == rs && pe == rs + vpr) {
+        out_v[r * k + lane] = lv;
+        out_i[r * k + lane] = li;
+      } else {
+        const long long slot = 2 * w + (ps == v0 ? 0 : 1);
+        part_v[slot * k + lane] = lv;
+        part_i[slot * k + lane] = li;
+      }
+    }
+    lv = tv = bar = -INFINITY;
+    li = ti = INT32_MAX;
+    fresh = true;
+  };
+
+  // the next batch's loads are issued before this batch is scanned
+  uint4 nq[kTsUnroll];
+#pragma unroll
+  for (int u = 0; u < kTsUnroll; ++u)
+    if (v0 + lane + 32 * u < v1) nq[u] = __ldcs(xv + v0 + lane + 32 * u);
+  for (long long b0 = v0; b0 < v1; b0 += kBatch) {
+    const int lim = (int)min((long long)kBatch, v1 - b0);
+    uint4 q[kTsUnroll];
+#pragma unroll
+    for (int u = 0; u < kTsUnroll; ++u) q[u] = nq[u];
+    const long long b1 = b0 + kBatch;
+#pragma unroll
+    for (int u = 0; u < kTsUnroll; ++u)
+      if (b1 + lane + 32 * u < v1) nq[u] = __ldcs(xv + b1 + lane + 32 * u);
+    if (fresh && lim <= rs + vpr - b0) {
+      // the first batch of a row piece lies in one row: its lanes' maxima are
+      // 32 distinct values of the piece, so the k-th largest of them bounds the
+      // piece's k-th largest from below
+      float lm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kTsUnroll; ++u)
+        if (lane + 32 * u < lim) lm = fmaxf(lm, vec_max<T>(q[u]));
+      unsigned key = lm == lm ? score_key(lm) : 0u;
+      unsigned kth = 0;
+      for (int j = 0; j < k; ++j) {
+        kth = __reduce_max_sync(0xffffffffu, key);
+        const unsigned hit = __ballot_sync(0xffffffffu, key == kth);
+        if (lane == __ffs(hit) - 1) key = 0;  // each lane maximum counts once
+      }
+      if (kth != 0) bar = score_unkey(kth);
+    }
+    fresh = false;
+    int ps = 0;  // piece [ps, pe) of this batch lies in row r (offsets from b0)
+    while (ps < lim) {
+      const int pe = (int)min((long long)lim, rs + vpr - b0);
+      const int base = (int)((b0 - rs) * E);  // row-local index of vector b0
+#pragma unroll
+      for (int u = 0; u < kTsUnroll; ++u) {
+        const int j = lane + 32 * u;
+        const bool in = j >= ps && j < pe;
+        const float m = vec_max<T>(q[u]);
+        const bool flag = in && (m > tv || ti == INT32_MAX) && !(m < bar);
+        const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+        if (ballot) take_flagged<T>(ballot, q[u], base + j * E, k, lv, li, tv, ti);
+      }
+      if (b0 + pe == rs + vpr) {
+        emit(b0 + pe);
+        ++r;
+        rs += vpr;
+      }
+      ps = pe;
+    }
+  }
+  if (v1 > rs && v1 < rs + vpr) emit(v1);  // the range ends inside row r
+}
+
+// Rows cut by range boundaries: warp p-1 of the grid owns boundary p when p is
+// the first boundary inside its row, and folds that row's pieces.
+__global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
+                                         const int32_t *__restrict__ part_i, long long nv,
+                                         long long vpr, long long owners, int k,
+                                         float *__restrict__ out_v, int32_t *__restrict__ out_i) {
+  const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5) + 1;
+  const int lane = threadIdx.x & 31;
+  if (p >= owners) return;
+  const long long bnd = ts_split(p, nv, owners);
+  const long long r = bnd / vpr, rs = r * vpr;
+  if (bnd == rs) return;                          // on a row start: nothing cut
+  if (ts_split(p - 1, nv, owners) > rs) return;   // an earlier boundary owns this row
+  const long long c0 = p - 1;
+  const long long xl = rs + vpr - 1;              // owner of the row's last vector:
+  const long long c1 = ((xl + 1) * owners + nv - 1) / nv - 1;  // ceil((x+1)*owners/nv) - 1
+  float lv = -INFINITY;
+  int li = INT32_MAX;
+  for (long long c = c0; c <= c1; ++c) {
+    const long long s0 = ts_split(c, nv, owners);
+    if (s0 == ts_split(c + 1, nv, owners)) continue;  // empty range
+    const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
+    for (int j = 0; j < k; ++j) {
+      const int xi = part_i[slot * k + j];
+      if (xi == INT32_MAX) break;
+      wl_insert(lv, li, part_v[slot * k + j], xi);
+    }
+  }
+  if (lane < k) {
+    out_v[r * k + lane] = lv;
+    out_i[r * k + lane] = li;
+  }
+}
+
+// ------------------------------------------------------------------ planning
 
 struct TopkPlan {
-  int chunks;
+  bool stream;
+  int chunks;      // chunk plan
   int chunk_len;
+  int ctas;        // stream plan
+  size_t pairs;    // partial (value, index) pairs the plan writes
 };
 
-TopkPlan plan_topk(long long rows, long long V, int esize) {
+bool topk_stream_shape(long long rows, long long V, int esize) {
+  return (V * esize) % 16 == 0 && rows * V * esize >= 32768LL * sm_count();
+}
+
+TopkPlan topk_chunk_plan(long long rows, long long V, int esize, int k) {
   const int E = 16 / esize;
   // a few thread blocks per SM; never cut a row below 32K elements
   const long long want = 8LL * sm_count();
@@ -261,7 +461,25 @@ TopkPlan plan_topk(long long rows, long long V, int esize) {
   long long len = (V + chunks - 1) / chunks;
   len = (len + E - 1) / E * E;
   chunks = (V + len - 1) / len;
-  return TopkPlan{(int)chunks, (int)len};
+  return TopkPlan{false, (int)chunks, (int)len, 0,
+                  chunks > 1 ? (size_t)rows * chunks * k : (size_t)0};
+}
+
+TopkPlan plan_topk(const void *x, long long rows, long long V, long long row_stride, int esize,
+                   int k) {
+  if (topk_stream_shape(rows, V, esize) && row_stride == V &&
+      (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+    const int ctas = sm_count();
+    return TopkPlan{true, 1, 0, ctas, (size_t)2 * ctas * kTsWarps * k};
+  }
+  return topk_chunk_plan(rows, V, esize, k);
+}
+
+size_t topk_workspace_pairs(long long rows, long long V, int esize, int k) {
+  size_t n = topk_chunk_plan(rows, V, esize, k).pairs;
+  if (topk_stream_shape(rows, V, esize))
+    n = n > (size_t)2 * sm_count() * kTsWarps * k ? n : (size_t)2 * sm_count() * kTsWarps * k;
+  return n;
 }
 
 // ------------------------------------------------------------------ build_tree
@@ -269,21 +487,40 @@ TopkPlan plan_topk(long long rows, long long V, int esize) {
 constexpr int kBtWarps = 4;
 constexpr int kBtStreams = TV_MAX_NODES + 1;  // the roots' cursor + one per node
 constexpr int kBtSlots = (kBtStreams + 31) / 32;
+constexpr int kBtStage = 1024;                // candidate tables up to L*K entries in smem
 
 struct BtWarp {
   float node_score[TV_MAX_NODES];
   int node_tok[TV_MAX_NODES];
   int node_par[TV_MAX_NODES];
   int node_dep[TV_MAX_NODES];
-  int next[kBtStreams];   // next child rank of the cursor, -1 while closed
-  int cbase[kBtStreams];  // push counter of the cursor's rank-0 candidate
+  float lp[kBtStage];     // this sequence's candidate log-probs (when L*K fits)
+  int tk[kBtStage];       // and token ids
 };
 
+
+// Candidate of a cursor at its current rank (key 0 once it runs past K).
+__device__ __forceinline__ void bt_refresh(const float *lp, int K, int nr, int cb, int dep,
+                                           float base, unsigned &key, int &cnt, float &sc) {
+  if (nr >= 0 && nr < K) {
+    const float v = lp[(size_t)(dep - 1) * K + nr];
+    sc = dep == 1 ? v : __fadd_rn(base, v);
+    key = score_key(sc);
+    cnt = cb + nr;
+  } else {
+    key = 0;
+  }
+}
+
+// Cursor u of a lane is stream lane + 32u: stream 0 walks the roots, stream
+// t+1 the children of node t.  A lane keeps its cursors' state in registers:
+// next rank, push counter of rank 0, the parent's score and the candidate
+// depth, and the current candidate's score key and counter (key 0: none).
 __global__ void __launch_bounds__(32 * kBtWarps)
-build_tree_kernel(const float *__restrict__ cand_lp, const int32_t *__restrict__ cand_idx, int B,
-                  int L, int K, int budget, int w, int32_t *__restrict__ tokens,
-                  int32_t *__restrict__ parent, int32_t *__restrict__ depth,
-                  float *__restrict__ score, int32_t *__restrict__ n_nodes) {
+build_tree_kernel(const float *cand_lp, const int32_t *cand_idx, int B, int L, int K, int budget,
+                  int w, int32_t *__restrict__ tokens, int32_t *__restrict__ parent,
+                  int32_t *__restrict__ depth, float *__restrict__ score,
+                  int32_t *__restrict__ n_nodes) {
   __shared__ BtWarp sh[kBtWarps];
   const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * kBtWarps + wid;
@@ -291,73 +528,108 @@ build_tree_kernel(const float *__restrict__ cand_lp, const int32_t *__restrict__
   BtWarp &s = sh[wid];
   const float *lp = cand_lp + (size_t)b * L * K;
   const int32_t *tk = cand_idx + (size_t)b * L * K;
-  for (int j = lane; j < kBtStreams; j += 32) {
-    s.next[j] = j == 0 ? 0 : -1;
-    s.cbase[j] = 0;
+  if (L * K <= kBtStage) {  // every pop reads these: keep them next to the warp
+    for (int j0 = 0; j0 < L * K; j0 += 128) {  // four loads per lane in flight, then stores
+      float v[4];
+      int t[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = j0 + lane + 32 * i;
+        if (j < L * K) {
+          v[i] = __ldg(lp + j);
+          t[i] = __ldg(tk + j);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = j0 + lane + 32 * i;
+        if (j < L * K) {
+          s.lp[j] = v[i];
+          s.tk[j] = t[i];
+        }
+      }
+    }
+    lp = s.lp;
+    tk = s.tk;
+    __syncwarp();
   }
-  __syncwarp();
-  int counter = K;  // the K roots took counters 0 .. K-1
+  int nr[kBtSlots], cb[kBtSlots], dep[kBtSlots];
+  float base[kBtSlots];
+  unsigned key[kBtSlots];
+  int cnt[kBtSlots];
+  float sc[kBtSlots];
+#pragma unroll
+  for (int u = 0; u < kBtSlots; ++u) {
+    nr[u] = -1;
+    cb[u] = 0;
+    dep[u] = 1;
+    base[u] = 0.f;
+    key[u] = 0;
+    cnt[u] = INT32_MAX;
+    sc[u] = -INFINITY;
+  }
+  if (lane == 0) {  // the roots: depth-1 candidates, counters 0 .. K-1
+    nr[0] = 0;
+    cb[0] = 0;
+    dep[0] = 1;
+    base[0] = 0.f;
+    bt_refresh(lp, K, nr[0], cb[0], dep[0], base[0], key[0], cnt[0], sc[0]);
+  }
+  int counter = K;
   int n = 0;
   while (n < budget) {
     const int start = n;
     const int take = min(w, budget - n);
     for (int q = 0; q < take; ++q) {
-      // every lane evaluates its cursors; then a warp-wide arg-max
-      float bs = -INFINITY;
-      int bc = INT32_MAX, bstream = -1;
+      // this lane's best cursor: higher score, then lower counter
+      unsigned bk = 0;
+      int bc = INT32_MAX, bu = -1;
 #pragma unroll
-      for (int u = 0; u < kBtSlots; ++u) {
-        const int st = lane + 32 * u;
-        if (st >= kBtStreams) break;
-        const int r = s.next[st];
-        if (r < 0 || r >= K) continue;
-        const int d = st == 0 ? 1 : s.node_dep[st - 1] + 1;  // candidate depth
-        const float sc = st == 0 ? lp[r] : __fadd_rn(s.node_score[st - 1], lp[(size_t)(d - 1) * K + r]);
-        const int cn = s.cbase[st] + r;
-        if (bstream < 0 || sc > bs || (sc == bs && cn < bc)) {
-          bs = sc;
-          bc = cn;
-          bstream = st;
+      for (int u = 0; u < kBtSlots; ++u)
+        if (key[u] > bk || (key[u] == bk && key[u] != 0 && cnt[u] < bc)) {
+          bk = key[u];
+          bc = cnt[u];
+          bu = u;
+        }
+      const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
+      if (wk == 0) break;  // the heap ran empty: the round ends early
+      const unsigned wc = __reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bc : 0xffffffffu);
+      const unsigned win = __ballot_sync(0xffffffffu, bk == wk && (unsigned)bc == wc);
+      if (lane == __ffs(win) - 1) {
+#pragma unroll
+        for (int u = 0; u < kBtSlots; ++u) {  // static indices keep the cursors in registers
+          if (u == bu) {
+            s.node_score[n] = sc[u];
+            s.node_tok[n] = tk[(size_t)(dep[u] - 1) * K + nr[u]];
+            s.node_par[n] = lane + 32 * u - 1;
+            s.node_dep[n] = dep[u];
+            ++nr[u];
+            bt_refresh(lp, K, nr[u], cb[u], dep[u], base[u], key[u], cnt[u], sc[u]);
+          }
         }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        const int ost = __shfl_xor_sync(0xffffffffu, bstream, o);
-        if (ost >= 0 && (bstream < 0 || os > bs || (os == bs && oc < bc))) {
-          bs = os;
-          bc = oc;
-          bstream = ost;
-        }
-      }
-      if (bstream < 0) break;  // the heap ran empty: the round ends early
-      if (lane == 0) {
-        const int r = s.next[bstream];
-        const int d = bstream == 0 ? 1 : s.node_dep[bstream - 1] + 1;
-        s.node_score[n] = bs;
-        s.node_tok[n] = tk[(size_t)(d - 1) * K + r];
-        s.node_par[n] = bstream - 1;
-        s.node_dep[n] = d;
-        s.next[bstream] = r + 1;
-      }
-      __syncwarp();
       ++n;
     }
     if (n == start) break;  // nothing left to pop: the K-ary tree of depth L is complete
-    // after the round, the round's nodes push their children, in pop order
-    if (lane == 0) {
-      for (int t = start; t < n; ++t) {
-        if (s.node_dep[t] < L) {
-          s.next[t + 1] = 0;
-          s.cbase[t + 1] = counter;
-          counter += K;
-        }
+    __syncwarp();
+    // after the round, its nodes push their children, in pop order: node t
+    // (depth < L) opens cursor t+1 with the next K push counters
+#pragma unroll
+    for (int u = 0; u < kBtSlots; ++u) {
+      const int t = lane + 32 * u - 1;
+      if (t >= start && t < n && s.node_dep[t] < L) {
+        int before = 0;
+        for (int t2 = start; t2 < t; ++t2) before += s.node_dep[t2] < L;
+        nr[u] = 0;
+        cb[u] = counter + K * before;
+        dep[u] = s.node_dep[t] + 1;
+        base[u] = s.node_score[t];
+        bt_refresh(lp, K, nr[u], cb[u], dep[u], base[u], key[u], cnt[u], sc[u]);
       }
     }
-    counter = __shfl_sync(0xffffffffu, counter, 0);
-    __syncwarp();
+    for (int t = start; t < n; ++t) counter += s.node_dep[t] < L ? K : 0;
   }
+  __syncwarp();
   for (int t = lane; t < budget; t += 32) {
     const size_t o = (size_t)b * budget + t;
     const bool real = t < n;
@@ -378,9 +650,8 @@ using namespace tv;
 extern "C" size_t tv_topk_workspace_size(int64_t rows, int64_t V, int k, int dtype) {
   if (rows <= 0 || V <= 0 || k < 1 || k > TV_TOPK_MAX) return 0;
   const int esize = dtype == TV_F32 ? 4 : 2;
-  const TopkPlan p = plan_topk(rows, V, esize);
-  if (p.chunks == 1) return 0;
-  const size_t n = (size_t)rows * p.chunks * k;
+  const size_t n = topk_workspace_pairs(rows, V, esize, k);
+  if (n == 0) return 0;
   return ((n * sizeof(float) + 255) / 256) * 256 + n * sizeof(int32_t);
 }
 
@@ -394,31 +665,51 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
   if (rows > (int64_t)INT32_MAX) return TV_ERR_ARG;
   if (!x || !out_vals || !out_idx) return TV_ERR_ARG;
   const int esize = dtype == TV_F32 ? 4 : 2;
-  const TopkPlan p = plan_topk(rows, V, esize);
-  if ((long long)rows * p.chunks > (long long)INT32_MAX) return TV_ERR_ARG;
+  const TopkPlan p = plan_topk(x, rows, V, row_stride, esize, k);
+  if (!p.stream && (long long)rows * p.chunks > (long long)INT32_MAX) return TV_ERR_ARG;
   float *pv = out_vals;
   int32_t *pi = out_idx;
-  if (p.chunks > 1) {
+  if (p.pairs > 0) {
     if (!workspace || workspace_bytes < tv_topk_workspace_size(rows, V, k, dtype)) return TV_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(workspace) & 15) return TV_ERR_ARG;
-    const size_t n = (size_t)rows * p.chunks * k;
+    const size_t n = topk_workspace_pairs(rows, V, esize, k);
     pv = static_cast<float *>(workspace);
     pi = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) +
                                      ((n * sizeof(float) + 255) / 256) * 256);
   }
+  cudaStream_t s = as_stream(stream);
+  if (p.stream) {
+    const long long vpr = V * esize / 16;
+    const long long nv = rows * vpr;
+    const long long owners = (long long)p.ctas * kTsWarps;
+    if (dtype == TV_BF16)
+      topk_stream_kernel<__nv_bfloat16><<<p.ctas, 32 * kTsWarps, 0, s>>>(
+          static_cast<const __nv_bfloat16 *>(x), nv, vpr, owners, k, pv, pi, out_vals, out_idx);
+    else
+      topk_stream_kernel<float><<<p.ctas, 32 * kTsWarps, 0, s>>>(
+          static_cast<const float *>(x), nv, vpr, owners, k, pv, pi, out_vals, out_idx);
+    const int wpb = 8;
+    topk_stream_merge_kernel<<<(unsigned)((owners - 1 + wpb - 1) / wpb), 32 * wpb, 0, s>>>(
+        pv, pi, nv, vpr, owners, k, out_vals, out_idx);
+    return launch_status();
+  }
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((row_stride * esize) % 16 == 0);
   const unsigned grid = (unsigned)(rows * p.chunks);
-  cudaStream_t s = as_stream(stream);
+  float *cv = p.chunks > 1 ? pv : out_vals;
+  int32_t *ci = p.chunks > 1 ? pi : out_idx;
   if (dtype == TV_BF16)
     topk_chunk_kernel<__nv_bfloat16><<<grid, kTopThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16 *>(x), (int)V, row_stride, p.chunks, p.chunk_len, vec, k, pv,
-        pi);
+        static_cast<const __nv_bfloat16 *>(x), (int)V, row_stride, p.chunks, p.chunk_len, vec, k, cv,
+        ci);
   else
     topk_chunk_kernel<float><<<grid, kTopThreads, 0, s>>>(static_cast<const float *>(x), (int)V,
                                                           row_stride, p.chunks, p.chunk_len, vec, k,
-                                                          pv, pi);
-  if (p.chunks > 1)
-    topk_merge_kernel<<<(unsigned)rows, kTopThreads, 0, s>>>(pv, pi, p.chunks, k, out_vals, out_idx);
+                                                          cv, ci);
+  if (p.chunks > 1) {
+    const int wpb = 8;
+    topk_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), 32 * wpb, 0, s>>>(pv, pi, rows, p.chunks,
+                                                                            k, out_vals, out_idx);
+  }
   return launch_status();
 }
 
