@@ -46,8 +46,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
-    ap.add_argument("--path", choices=["verify", "draft"], default="verify",
-                    help="verify: the verify step (default); draft: draft-tree construction")
+    ap.add_argument("--path", choices=["verify", "draft", "graph"], default="verify",
+                    help="verify: the verify step (default); draft: draft-tree construction; "
+                         "graph: the multi-layer step, eager launches vs one CUDA-graph replay")
+    ap.add_argument("--layers", type=int, default=8, help="attention layers for --path graph")
     ap.add_argument("--draft-workload", default="tree_build")
     return ap.parse_args()
 
@@ -343,6 +345,8 @@ def bench_ours(args, rank, world, local):
         d = measure_draft("tree_build", 50, 3, dev)
         d.pop("_inputs")
         line["draft_path"] = d
+        # the multi-layer step as one CUDA-graph replay, on the small best-first batch
+        line["graph_path"] = measure_graph("best_first", 8, 50, 3, dev)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
     return line
@@ -515,6 +519,77 @@ def bench_draft(args, rank, world, local):
     return line
 
 
+GRAPH_METRIC = "multi-layer verify steps/s: one CUDA-graph replay vs eager launches"
+
+
+def measure_graph(name, layers, steps, warmup, dev, batch=None, seed_offset=0):
+    """The L-layer step (ModelStep) on one GPU: eager launches and graph
+    replays, each timed with CUDA events over `steps` steps."""
+    import torch
+    import workloads
+    import tree_speculative_decoding_build_gb300 as tv
+    w = workloads.get(name)
+    inp = workloads.make(name, dev, seed=w.seed + seed_offset, B=batch, plant="path")
+    lys = workloads.make_layers(inp, layers, seed=w.seed + seed_offset)
+    ms = tv.ModelStep(inp, lys, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        for _ in range(max(3, warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / steps
+
+    eager_ms = timed(lambda: ms.run())
+    ms.capture()
+    graph_ms = timed(lambda: ms.replay())
+    launches = ms.launches
+    ok = int(ms.out.status.abs().sum()) == 0
+    ms.close()
+    per_layer = attention_algorithmic_bytes(inp)
+    return {
+        "workload": (f"{name}: B={inp['B']} N={inp['N']} Hq/Hkv/D={inp['Hq']}/{inp['Hkv']}/"
+                     f"{inp['D']}, {layers} layers (own q/k/v/caches each), V={inp['V']}"),
+        "layers": layers, "eager_ms_per_step": eager_ms, "graph_ms_per_step": graph_ms,
+        "graph_speedup": eager_ms / graph_ms, "launches_per_step": launches,
+        "attention_bytes_per_step": per_layer * layers, "status_ok": ok,
+    }
+
+
+def bench_graph(args, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    r = measure_graph(name, args.layers, args.steps, args.warmup, dev, batch=args.batch,
+                      seed_offset=rank)
+    ms = max_over_ranks(r["graph_ms_per_step"], world, dev)
+    if rank != 0:
+        return None
+    peak, peak_kind = peaks()
+    gbs = r["attention_bytes_per_step"] / (ms * 1e-3) / 1e9
+    return {
+        "metric": GRAPH_METRIC, "value": job_throughput(world, 1, ms), "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "impl": "ours", "path": "graph",
+        "config": {"workload": r["workload"], "l2": "inputs larger than L2"},
+        "eager": {"ms_per_step": r["eager_ms_per_step"], "value": 1000.0 / r["eager_ms_per_step"]},
+        "graph_speedup": r["graph_speedup"],
+        "roofline": {"kernel": "whole step (all layers)", "bound": "hbm", "achieved": gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+                     "peak_source": peak_kind},
+        "gpu_launches": r["launches_per_step"] * args.steps, "status_ok": r["status_ok"],
+    }
+
+
 def oracle_step_sample(npi, heads):
     """One verify step of the oracle on a one-sequence input, attention limited
     to the first ``heads`` query heads.  Returns (attention seconds, rest seconds)."""
@@ -608,6 +683,8 @@ def main():
         dist.init_process_group("nccl")
     if args.path == "draft":
         line = bench_draft(args, rank, world, local)
+    elif args.path == "graph":
+        line = bench_graph(args, rank, world, local)
     else:
         line = bench_ours(args, rank, world, local)
     if line is not None:

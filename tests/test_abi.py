@@ -112,3 +112,22 @@ def test_draft_host_argument_checks(lib):
     lib.tv_topk_workspace_size.argtypes = [L, L, I, I]
     lib.tv_topk_workspace_size.restype = S
     assert lib.tv_topk_workspace_size(1, 8, 0, 0) == 0
+
+
+def test_graph_host_argument_checks(lib):
+    P = ctypes.c_void_p
+    lib.tv_verify_step.argtypes = [P, P]
+    lib.tv_verify_step.restype = ctypes.c_int
+    assert lib.tv_verify_step(None, None) == 1
+    lib.tv_verify_graph_create.argtypes = [P, ctypes.POINTER(P)]
+    lib.tv_verify_graph_create.restype = ctypes.c_int
+    h = P()
+    assert lib.tv_verify_graph_create(None, ctypes.byref(h)) == 1 and not h.value
+    assert lib.tv_verify_graph_create(None, None) == 1
+    lib.tv_verify_graph_launch.argtypes = [P, P]
+    lib.tv_verify_graph_launch.restype = ctypes.c_int
+    assert lib.tv_verify_graph_launch(None, None) == 1
+    lib.tv_verify_graph_launches.argtypes = [P]
+    assert lib.tv_verify_graph_launches(None) == 0
+    lib.tv_verify_graph_destroy.argtypes = [P]
+    lib.tv_verify_graph_destroy(None)

@@ -8,6 +8,10 @@ bound here through ctypes with the same names:
 ``VerifyStep`` owns the output and scratch buffers of one batch shape and
 enqueues the five calls on one CUDA stream with no host synchronisation.
 
+``ModelStep`` (``include/tv_graph.h``) is the step of an L-layer model: every
+layer's attention and commit in one unit, enqueued eagerly or captured once
+into a CUDA graph and replayed, so nothing runs eagerly between replays.
+
 The draft side (``include/tv_draft.h``) builds the tree the step verifies:
 ``tv_topk`` gives each draft position's candidate list and ``tv_build_tree``
 expands them best-first into tokens / parent / depth.  ``DraftTree`` owns the
@@ -24,7 +28,9 @@ from ._lib import (  # noqa: F401
     TV_ERR_CUDA, TV_ERR_SCRATCH_LIMIT, TV_ERR_TREE, TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError,
     status_string, tv_argmax, tv_argmax_noalloc, tv_argmax_workspace_size, tv_build_ancestors,
     tv_build_tree, tv_commit_kv, tv_topk, tv_topk_workspace_size, tv_tree_attention,
-    tv_tree_attention_workspace_size, tv_tree_walk)
+    tv_tree_attention_workspace_size, tv_tree_walk, tv_verify_graph_create,
+    tv_verify_graph_destroy, tv_verify_graph_launch, tv_verify_graph_launches, tv_verify_step)
+from ._lib import step_args as _step_args
 
 
 @dataclasses.dataclass
@@ -87,6 +93,75 @@ class VerifyStep:
                      inp["block_table"], inp["k_cache"], inp["v_cache"], o.ctx_len_out, o.status,
                      stream)
         return o
+
+
+class ModelStep:
+    """The verify step of an L-layer model for fixed buffers: tv_build_ancestors,
+    every layer's tv_tree_attention, tv_argmax, tv_tree_walk, every layer's
+    tv_commit_kv.  ``inp`` holds the tree, sequence state and logits (the dict
+    of ``workloads.make``), ``layers`` one dict per layer with q / k_tree /
+    v_tree / k_cache / v_cache tensors; each layer's attention output is
+    allocated here (``self.attn[l]``).  ``run()`` enqueues the launches
+    eagerly; ``capture()`` records them once into a CUDA graph, after which
+    ``replay()`` launches the graph.  Buffers are used in place: refill them
+    between replays."""
+
+    def __init__(self, inp, layers, device="cuda"):
+        dev = torch.device(device)
+        B, N, Hq, Hkv, D = inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"]
+        V = inp["logits"].shape[-1]
+        i32 = torch.int32
+        self.inp = inp
+        self.out = StepOutputs(
+            anc=torch.empty((B, N), dtype=torch.int64, device=dev),
+            pos=torch.empty((B, N), dtype=i32, device=dev),
+            status=torch.empty((B,), dtype=i32, device=dev),
+            attn=torch.empty((0,), dtype=torch.bfloat16, device=dev),
+            argmax=torch.empty((B, N), dtype=i32, device=dev),
+            out_tokens=torch.empty((B, N + 1), dtype=i32, device=dev),
+            n_emit=torch.empty((B,), dtype=i32, device=dev),
+            acc_nodes=torch.empty((B, N), dtype=i32, device=dev),
+            n_acc=torch.empty((B,), dtype=i32, device=dev),
+            ctx_len_out=torch.empty((B,), dtype=i32, device=dev))
+        self.attn = [torch.empty((B, N, Hq, D), dtype=torch.bfloat16, device=dev) for _ in layers]
+        self.layers = [dict(ly, out=o) for ly, o in zip(layers, self.attn)]
+        ws_attn = tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, inp["max_blocks"],
+                                                   inp["window_left"])
+        dt = TV_F32 if inp["logits"].dtype == torch.float32 else TV_BF16
+        ws_arg = tv_argmax_workspace_size(B * N, V, dt)
+        self.ws_attn = torch.empty(max(ws_attn, 1), dtype=torch.uint8, device=dev)
+        self.ws_arg = torch.empty(max(ws_arg, 1), dtype=torch.uint8, device=dev)
+        flat = dict(inp, logits=inp["logits"].reshape(B * N, V))
+        self.args = _step_args(flat, self.out, self.layers, self.ws_attn, self.ws_arg)
+        self.graph = None
+
+    def run(self, stream=None):
+        tv_verify_step(self.args, stream)
+        return self.out
+
+    def capture(self):
+        if self.graph is None:
+            self.graph = tv_verify_graph_create(self.args)
+        return self
+
+    def replay(self, stream=None):
+        tv_verify_graph_launch(self.graph, stream)
+        return self.out
+
+    @property
+    def launches(self):
+        return tv_verify_graph_launches(self.graph) if self.graph is not None else None
+
+    def close(self):
+        if self.graph is not None:
+            tv_verify_graph_destroy(self.graph)
+            self.graph = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 @dataclasses.dataclass

@@ -1,7 +1,7 @@
 """ctypes binding of libtv.so: argument marshalling only.
 
 Each ``tv_*`` function here has the name and argument order of the C entry
-point in ``include/tv.h`` or ``include/tv_draft.h``; it checks dtypes, devices and contiguity of the
+point in ``include/tv.h``, ``include/tv_draft.h`` or ``include/tv_graph.h``; it checks dtypes, devices and contiguity of the
 torch tensors it is given, passes their device pointers, and raises
 ``TvError`` on a non-zero host status.  All arithmetic runs in the library's
 CUDA kernels; there is no fallback of any kind: without the compiled library
@@ -39,6 +39,11 @@ EXPORTS = (
     "tv_topk_workspace_size",
     "tv_topk",
     "tv_build_tree",
+    "tv_verify_step",
+    "tv_verify_graph_create",
+    "tv_verify_graph_launch",
+    "tv_verify_graph_launches",
+    "tv_verify_graph_destroy",
 )
 
 
@@ -60,6 +65,32 @@ class AttnArgs(ctypes.Structure):
         ("num_blocks", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
         ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("kernel", ctypes.c_int),
         ("out", ctypes.c_void_p), ("status", ctypes.c_void_p),
+    ]
+
+
+class Layer(ctypes.Structure):
+    """Mirror of ``tv_layer``."""
+    _fields_ = [("q", ctypes.c_void_p), ("k_tree", ctypes.c_void_p), ("v_tree", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+
+
+class StepArgs(ctypes.Structure):
+    """Mirror of ``tv_step_args``."""
+    _fields_ = [
+        ("tokens", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("depth", ctypes.c_void_p),
+        ("ctx_len", ctypes.c_void_p), ("root_pred", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("B", ctypes.c_int), ("N", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
+        ("D", ctypes.c_int), ("max_blocks", ctypes.c_int), ("num_blocks", ctypes.c_int),
+        ("window_left", ctypes.c_int), ("sm_scale", ctypes.c_float),
+        ("num_layers", ctypes.c_int), ("layers", ctypes.POINTER(Layer)),
+        ("attn_workspace", ctypes.c_void_p), ("attn_workspace_bytes", ctypes.c_size_t),
+        ("logits", ctypes.c_void_p), ("logits_dtype", ctypes.c_int), ("V", ctypes.c_int64),
+        ("argmax_workspace", ctypes.c_void_p), ("argmax_workspace_bytes", ctypes.c_size_t),
+        ("anc", ctypes.c_void_p), ("pos", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("argmax", ctypes.c_void_p), ("out_tokens", ctypes.c_void_p), ("n_emit", ctypes.c_void_p),
+        ("acc_nodes", ctypes.c_void_p), ("n_acc", ctypes.c_void_p),
+        ("ctx_len_out", ctypes.c_void_p),
     ]
 
 
@@ -87,8 +118,16 @@ def _load():
     lib.tv_topk_workspace_size.restype = S
     lib.tv_topk.argtypes = [P, I, L, L, L, I, P, P, P, S, P]
     lib.tv_build_tree.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
+    lib.tv_verify_step.argtypes = [ctypes.POINTER(StepArgs), P]
+    lib.tv_verify_graph_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(P)]
+    lib.tv_verify_graph_launch.argtypes = [P, P]
+    lib.tv_verify_graph_launches.argtypes = [P]
+    lib.tv_verify_graph_launches.restype = I
+    lib.tv_verify_graph_destroy.argtypes = [P]
+    lib.tv_verify_graph_destroy.restype = None
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
-              "tv_commit_kv", "tv_topk", "tv_build_tree"):
+              "tv_commit_kv", "tv_topk", "tv_build_tree", "tv_verify_step",
+              "tv_verify_graph_create", "tv_verify_graph_launch"):
         getattr(lib, f).restype = I
     return lib
 
@@ -291,3 +330,60 @@ def tv_build_tree(cand_lp, cand_idx, budget, w, tokens, parent, depth, score, n_
         int(budget), int(w), _ptr(tokens, i32, "tokens"), _ptr(parent, i32, "parent"),
         _ptr(depth, i32, "depth"), _ptr(score, torch.float32, "score"),
         _ptr(n_nodes, i32, "n_nodes"), _stream(stream)))
+
+
+def step_args(inp, out, layers, attn_ws, argmax_ws):
+    """A ``StepArgs`` for the tensors of one batch: ``inp`` holds the tree,
+    sequence state and logits (as produced by ``workloads.make``), ``out`` the
+    step outputs, ``layers`` a list of dicts with q / k_tree / v_tree / k_cache
+    / v_cache / out tensors.  The returned object keeps the layer array alive."""
+    i32, bf16 = torch.int32, torch.bfloat16
+    arr = (Layer * len(layers))()
+    for j, ly in enumerate(layers):
+        arr[j] = Layer(_ptr(ly["q"], bf16, "q"), _ptr(ly["k_tree"], bf16, "k_tree"),
+                       _ptr(ly["v_tree"], bf16, "v_tree"), _ptr(ly["k_cache"], bf16, "k_cache"),
+                       _ptr(ly["v_cache"], bf16, "v_cache"), _ptr(ly["out"], bf16, "out"))
+    lg = inp["logits"]
+    a = StepArgs(
+        tokens=_ptr(inp["tokens"], i32, "tokens"), parent=_ptr(inp["parent"], i32, "parent"),
+        depth=_ptr(inp["depth"], i32, "depth"), ctx_len=_ptr(inp["ctx_len"], i32, "ctx_len"),
+        root_pred=_ptr(inp["root_pred"], i32, "root_pred"),
+        block_table=_ptr(inp["block_table"], i32, "block_table"),
+        B=inp["B"], N=inp["N"], Hq=inp["Hq"], Hkv=inp["Hkv"], D=inp["D"],
+        max_blocks=inp["max_blocks"], num_blocks=layers[0]["k_cache"].shape[0],
+        window_left=inp["window_left"], sm_scale=0.0,
+        num_layers=len(layers), layers=arr,
+        attn_workspace=_ptr(attn_ws, None, "attn_workspace") if attn_ws is not None else None,
+        attn_workspace_bytes=attn_ws.numel() if attn_ws is not None else 0,
+        logits=_ptr(lg, None, "logits"), logits_dtype=_logits_dtype(lg), V=lg.shape[-1],
+        argmax_workspace=_ptr(argmax_ws, None, "argmax_workspace") if argmax_ws is not None else None,
+        argmax_workspace_bytes=argmax_ws.numel() if argmax_ws is not None else 0,
+        anc=_ptr(out.anc, torch.int64, "anc"), pos=_ptr(out.pos, i32, "pos"),
+        status=_ptr(out.status, i32, "status"), argmax=_ptr(out.argmax, i32, "argmax"),
+        out_tokens=_ptr(out.out_tokens, i32, "out_tokens"), n_emit=_ptr(out.n_emit, i32, "n_emit"),
+        acc_nodes=_ptr(out.acc_nodes, i32, "acc_nodes"), n_acc=_ptr(out.n_acc, i32, "n_acc"),
+        ctx_len_out=_ptr(out.ctx_len_out, i32, "ctx_len_out"))
+    a._layers = arr
+    return a
+
+
+def tv_verify_step(args, stream=None):
+    _check("tv_verify_step", lib.tv_verify_step(ctypes.byref(args), _stream(stream)))
+
+
+def tv_verify_graph_create(args):
+    h = ctypes.c_void_p()
+    _check("tv_verify_graph_create", lib.tv_verify_graph_create(ctypes.byref(args), ctypes.byref(h)))
+    return h
+
+
+def tv_verify_graph_launch(graph, stream=None):
+    _check("tv_verify_graph_launch", lib.tv_verify_graph_launch(graph, _stream(stream)))
+
+
+def tv_verify_graph_launches(graph):
+    return int(lib.tv_verify_graph_launches(graph))
+
+
+def tv_verify_graph_destroy(graph):
+    lib.tv_verify_graph_destroy(graph)

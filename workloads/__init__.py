@@ -491,3 +491,18 @@ def make_draft(name, device="cpu", seed: Optional[int] = None, *, B: Optional[in
     if quantum > 0:
         logits = torch.round(logits / quantum) * quantum
     return torch.log_softmax(logits, dim=-1).to(dtype)
+
+
+def make_layers(inp, num_layers: int, seed: int):
+    """Per-layer tensors of an L-layer model sharing ``inp``'s tree, block
+    table and logits: layer 0 is ``inp``'s own q / k_tree / v_tree / caches,
+    layers 1.. are fresh N(0, 1) bf16 tensors of the same shapes (seeded)."""
+    dev = inp["q"].device
+    layers = [dict(q=inp["q"], k_tree=inp["k_tree"], v_tree=inp["v_tree"],
+                   k_cache=inp["k_cache"], v_cache=inp["v_cache"])]
+    for l in range(1, num_layers):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed + 7777 * l)
+        layers.append({k: _randn_bf16(tuple(inp[k].shape), gen, dev)
+                       for k in ("q", "k_tree", "v_tree", "k_cache", "v_cache")})
+    return layers
