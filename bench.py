@@ -46,9 +46,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
-    ap.add_argument("--path", choices=["verify", "draft", "graph"], default="verify",
+    ap.add_argument("--path", choices=["verify", "draft", "graph", "gdn"], default="verify",
                     help="verify: the verify step (default); draft: draft-tree construction; "
-                         "graph: the multi-layer step, eager launches vs one CUDA-graph replay")
+                         "graph: the multi-layer step, eager launches vs one CUDA-graph replay; "
+                         "gdn: tree verification through a Gated DeltaNet layer + state commit")
     ap.add_argument("--layers", type=int, default=8, help="attention layers for --path graph")
     ap.add_argument("--draft-workload", default="tree_build")
     return ap.parse_args()
@@ -590,6 +591,115 @@ def bench_graph(args, rank, world, local):
     }
 
 
+GDN_METRIC = "GDN tree-verify steps/s (tv_gdn_tree_verify + tv_gdn_commit)"
+FP32_FMA_LANES_PER_SM = 128   # fp32 FMA lanes per SM (4 partitions x 32)
+
+
+def gdn_flops(x):
+    """Algorithmic flops of one verification: K S_0 and Q S_0 (2 x N x dk x dv
+    multiply-adds per value head), the ancestor-pair dot products, the solve and
+    the output sums (2 x pairs x dv each)."""
+    B, N, Hv, dk, dv = x["B"], x["N"], x["Hv"], x["dk"], x["dv"]
+    pairs = int(x["depth"].sum().item())  # over all sequences: sum of |ancestors-or-self|
+    return B * Hv * 2 * (2 * N * dk * dv) + Hv * (2 * (2 * pairs * dk) + 2 * (2 * pairs * dv))
+
+
+def gdn_bytes(x):
+    B, N, Hk, Hv, dk, dv = x["B"], x["N"], x["Hk"], x["Hv"], x["dk"], x["dv"]
+    return (B * Hv * dv * dk * 4 + 2 * B * N * Hk * dk * 2 + B * N * Hv * dv * 2 + 2 * B * N * Hv * 4
+            + 2 * B * N * Hv * dv * 4 + B * N * Hv * 4 + B * N * 8)
+
+
+def measure_gdn(name, steps, warmup, dev, batch=None, seed_offset=0):
+    import torch
+    import workloads
+    import tree_speculative_decoding_build_gb300 as tv
+    w = workloads.GDN_WORKLOADS[name]
+    x = workloads.make_gdn(name, dev, seed=w.seed + seed_offset, B=batch)
+    B, N, Hv, dv = x["B"], x["N"], x["Hv"], x["dv"]
+    anc = torch.empty(B, N, dtype=torch.int64, device=dev)
+    pos = torch.empty(B, N, dtype=torch.int32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+    ctx = torch.full((B,), 1000, dtype=torch.int32, device=dev)
+    tv.tv_build_ancestors(x["parent"], x["depth"], ctx, anc, pos, st)
+    out = torch.empty(B, N, Hv, dv, device=dev)
+    u = torch.empty_like(out)
+    g = torch.empty(B, N, Hv, device=dev)
+    new = torch.empty_like(x["state"])
+    # accepted path per sequence: node 0's ancestors-or-self (a root) extended to its deepest child chain
+    acc = torch.zeros(B, N, dtype=torch.int32, device=dev)
+    n_acc = torch.ones(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tv.tv_gdn_tree_verify(x["state"], x["q"], x["k"], x["v"], x["alpha"], x["beta"], anc, out,
+                              u, g, st)
+        if ev is not None:
+            ev[1].record(stream)
+        tv.tv_gdn_commit(x["state"], x["k"], u, x["alpha"], acc, n_acc, new, st)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1) / steps
+    v_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    c_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    flops = gdn_flops(x)
+    sm_mhz = 2070.0
+    try:
+        sm_mhz = float(torch.cuda.get_device_properties(dev).clock_rate) / 1000.0 or sm_mhz
+    except Exception:
+        pass
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    alu_peak = sms * FP32_FMA_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12
+    commit_bytes = 2 * B * Hv * dv * x["dk"] * 4
+    return {
+        "workload": (f"{name}: B={B} N={N} Hk/Hv={x['Hk']}/{x['Hv']} dk/dv={x['dk']}/{dv}, "
+                     f"fp32 state, bf16 q/k/v"),
+        "ms_per_step": ms, "verify_ms": v_ms, "commit_ms": c_ms,
+        "verify_tflops": flops / (v_ms * 1e-3) / 1e12, "verify_flops": flops,
+        "verify_bytes": gdn_bytes(x), "fp32_peak_tflops": alu_peak, "sm_mhz_for_peak": sm_mhz,
+        "commit_gbs": commit_bytes / (c_ms * 1e-3) / 1e9, "status_ok": int(st.abs().sum()) == 0,
+    }
+
+
+def bench_gdn(args, rank, world, local):
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = measure_gdn("gdn_stress", args.steps, args.warmup, dev, batch=args.batch,
+                    seed_offset=rank)
+    ms = max_over_ranks(r["ms_per_step"], world, dev)
+    if rank != 0:
+        return None
+    return {
+        "metric": GDN_METRIC, "value": job_throughput(world, 1, ms), "unit": "steps/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "impl": "ours", "path": "gdn",
+        "config": {"workload": r["workload"], "l2": "state 134 MB read per step"},
+        "roofline": {"kernel": "tv_gdn_tree_verify", "bound": "alu",
+                     "achieved": r["verify_tflops"], "peak": r["fp32_peak_tflops"],
+                     "unit": "TFLOP/s", "frac": r["verify_tflops"] / r["fp32_peak_tflops"],
+                     "traffic": None,
+                     "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 flop x SM clock"},
+        "verify_ms": r["verify_ms"], "commit_ms": r["commit_ms"], "commit_gbs": r["commit_gbs"],
+        "gpu_launches": 2 * args.steps, "status_ok": r["status_ok"],
+    }
+
+
 def oracle_step_sample(npi, heads):
     """One verify step of the oracle on a one-sequence input, attention limited
     to the first ``heads`` query heads.  Returns (attention seconds, rest seconds)."""
@@ -685,6 +795,8 @@ def main():
         line = bench_draft(args, rank, world, local)
     elif args.path == "graph":
         line = bench_graph(args, rank, world, local)
+    elif args.path == "gdn":
+        line = bench_gdn(args, rank, world, local)
     else:
         line = bench_ours(args, rank, world, local)
     if line is not None:

@@ -12,6 +12,10 @@ enqueues the five calls on one CUDA stream with no host synchronisation.
 layer's attention and commit in one unit, enqueued eagerly or captured once
 into a CUDA graph and replayed, so nothing runs eagerly between replays.
 
+``tv_gdn_tree_verify`` / ``tv_gdn_commit`` (``include/tv_gdn.h``) verify a
+tree through a Gated DeltaNet layer without touching its state, then commit
+the state of the accepted path.
+
 The draft side (``include/tv_draft.h``) builds the tree the step verifies:
 ``tv_topk`` gives each draft position's candidate list and ``tv_build_tree``
 expands them best-first into tokens / parent / depth.  ``DraftTree`` owns the
@@ -28,7 +32,8 @@ from ._lib import (  # noqa: F401
     TV_ERR_CUDA, TV_ERR_SCRATCH_LIMIT, TV_ERR_TREE, TV_ERR_UNSUPPORTED, TV_F32, TV_OK, TvError,
     status_string, tv_argmax, tv_argmax_noalloc, tv_argmax_workspace_size, tv_build_ancestors,
     tv_build_tree, tv_commit_kv, tv_topk, tv_topk_workspace_size, tv_tree_attention,
-    tv_tree_attention_workspace_size, tv_tree_walk, tv_verify_graph_create,
+    tv_tree_attention_workspace_size, tv_tree_walk, tv_gdn_commit, tv_gdn_tree_verify,
+    tv_verify_graph_create,
     tv_verify_graph_destroy, tv_verify_graph_launch, tv_verify_graph_launches, tv_verify_step)
 from ._lib import step_args as _step_args
 

@@ -1,7 +1,7 @@
 """ctypes binding of libtv.so: argument marshalling only.
 
 Each ``tv_*`` function here has the name and argument order of the C entry
-point in ``include/tv.h``, ``include/tv_draft.h`` or ``include/tv_graph.h``; it checks dtypes, devices and contiguity of the
+point in ``include/tv.h``, ``tv_draft.h``, ``tv_graph.h`` or ``tv_gdn.h``; it checks dtypes, devices and contiguity of the
 torch tensors it is given, passes their device pointers, and raises
 ``TvError`` on a non-zero host status.  All arithmetic runs in the library's
 CUDA kernels; there is no fallback of any kind: without the compiled library
@@ -44,6 +44,8 @@ EXPORTS = (
     "tv_verify_graph_launch",
     "tv_verify_graph_launches",
     "tv_verify_graph_destroy",
+    "tv_gdn_tree_verify",
+    "tv_gdn_commit",
 )
 
 
@@ -125,9 +127,12 @@ def _load():
     lib.tv_verify_graph_launches.restype = I
     lib.tv_verify_graph_destroy.argtypes = [P]
     lib.tv_verify_graph_destroy.restype = None
+    lib.tv_gdn_tree_verify.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
+    lib.tv_gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
               "tv_commit_kv", "tv_topk", "tv_build_tree", "tv_verify_step",
-              "tv_verify_graph_create", "tv_verify_graph_launch"):
+              "tv_verify_graph_create", "tv_verify_graph_launch", "tv_gdn_tree_verify",
+              "tv_gdn_commit"):
         getattr(lib, f).restype = I
     return lib
 
@@ -387,3 +392,29 @@ def tv_verify_graph_launches(graph):
 
 def tv_verify_graph_destroy(graph):
     lib.tv_verify_graph_destroy(graph)
+
+
+def tv_gdn_tree_verify(state, q, k, v, alpha, beta, anc, out, u, g, status=None, stream=None):
+    """GDN outputs of every tree node from the committed state (include/tv_gdn.h).
+    state float32 [B, Hv, dv, dk] (S^T); q, k bf16 [B, N, Hk, dk]; v bf16
+    [B, N, Hv, dv]; alpha, beta float32 [B, N, Hv]; anc int64 [B, N]."""
+    B, N, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    f32, bf16 = torch.float32, torch.bfloat16
+    _check("tv_gdn_tree_verify", lib.tv_gdn_tree_verify(
+        _ptr(state, f32, "state"), _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"),
+        _ptr(alpha, f32, "alpha"), _ptr(beta, f32, "beta"), _ptr(anc, torch.int64, "anc"),
+        B, N, Hk, Hv, dk, dv, _ptr(out, f32, "out"), _ptr(u, f32, "u"), _ptr(g, f32, "g"),
+        _ptr(status, torch.int32, "status") if status is not None else None, _stream(stream)))
+
+
+def tv_gdn_commit(state_in, k, u, alpha, acc_nodes, n_acc, state_out, status=None, stream=None):
+    """The GDN state after the accepted path (include/tv_gdn.h)."""
+    B, N, Hk, dk = k.shape
+    Hv, dv = u.shape[2], u.shape[3]
+    f32, i32 = torch.float32, torch.int32
+    _check("tv_gdn_commit", lib.tv_gdn_commit(
+        _ptr(state_in, f32, "state_in"), _ptr(k, torch.bfloat16, "k"), _ptr(u, f32, "u"),
+        _ptr(alpha, f32, "alpha"), _ptr(acc_nodes, i32, "acc_nodes"), _ptr(n_acc, i32, "n_acc"),
+        B, N, Hk, Hv, dk, dv, _ptr(state_out, f32, "state_out"),
+        _ptr(status, i32, "status") if status is not None else None, _stream(stream)))

@@ -1,0 +1,417 @@
+// Rollback-free tree verification of a Gated DeltaNet layer, and the deferred
+// commit of its state.
+//
+// Source: "Technische Samenvatting: Trees from Marginals (DFlash-TfM)",
+// "3. Rollback-vrije Boom-verificatie voor GDN".  With u_t = beta_t (v_t -
+// alpha_t S_parent^T k_t) and g_t the product of alpha along a node's path,
+// the state of node t is S_t = g_t S_0 + sum_{i anc-or-self} (g_t/g_i) k_i u_i^T,
+// so the pseudo-values solve (I + X) U = beta * (V - g * K S_0), X masked to
+// strict ancestors (lower triangular in parents-first order), and the outputs
+// are O = g * (Q S_0) + Y U, Y masked to ancestors-or-self.
+//
+// tv_gdn_tree_verify: one CTA per (sequence, value head, 64 columns of d_v).
+// The columns of U are independent in the triangular system, so splitting d_v
+// only repeats the small ancestor-pair dot products.  In shared memory: the
+// 64 rows of S_0^T, K and Q rows of the key head (fp32, rows padded), X and Y
+// on ancestor pairs (one thread per pair), U's 64 columns.  For K S_0 and
+// Q S_0 (fp32 FMA, float4 shared loads, all loads of a step before its FMAs)
+// warp w owns rows t = w, w+8, ... and lane l columns l and l + 32.  For the
+// solve warp w owns 8 columns and all their rows, so its depth levels (a node
+// only needs its ancestors) are separated by warp syncs, not block barriers.
+// The path ratios g_t / g_i are products of alpha along the chain from i down
+// to t, so no division is made and deep paths cannot produce 0/0.
+//
+// tv_gdn_commit: one CTA per (sequence, value head, 32 rows of S^T): S_0 read
+// once, the accepted path's rank-n_acc update added, S written once.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "tv_gdn.h"
+
+namespace tv {
+namespace {
+
+constexpr int kGdnDC = 64;     // d_v columns per CTA (lane l owns l and l + 32)
+constexpr int kGcDC = 32;      // rows of S^T per commit CTA
+constexpr int kGdnWarps = 8;
+constexpr int kGdnThreads = 32 * kGdnWarps;
+constexpr int kGdnMaxN = 64;
+
+// 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+constexpr int kGdnRows = kGdnMaxN / kGdnWarps;  // rows per warp at most
+
+struct GdnLayout {
+  int N, dk;
+  size_t off_s, off_k, off_q, off_x, off_y, off_u, off_g, off_al, off_be, off_anc, off_par,
+      off_dep, bytes;
+};
+
+constexpr int kGdnUStride = kGdnDC + 1;  // U rows padded: the solve reads U down columns
+
+__host__ __device__ inline GdnLayout gdn_layout(int N, int dk) {
+  GdnLayout L;
+  L.N = N;
+  L.dk = dk;
+  size_t o = 0;
+  L.off_s = o; o += (size_t)kGdnDC * (dk + 4) * 4;
+  L.off_k = o; o += (size_t)N * (dk + 4) * 4;
+  L.off_q = o; o += (size_t)N * (dk + 4) * 4;
+  L.off_x = o; o += (size_t)N * (N + 1) * 4;
+  L.off_y = o; o += (size_t)N * (N + 1) * 4;
+  L.off_u = o; o += (size_t)N * kGdnUStride * 4;
+  L.off_g = o; o += (size_t)N * 4;
+  L.off_al = o; o += (size_t)N * 4;
+  L.off_be = o; o += (size_t)N * 4;
+  o = (o + 7) / 8 * 8;
+  L.off_anc = o; o += (size_t)N * 8;
+  L.off_par = o; o += (size_t)N * 4;
+  L.off_dep = o; o += (size_t)N * 4;
+  L.bytes = o + 16;
+  return L;
+}
+
+// ROWS: rows of the tree per warp in the K S_0 / Q S_0 product (N <= 8 * ROWS).
+template <int ROWS>
+__global__ void __launch_bounds__(kGdnThreads)
+gdn_tree_verify_kernel(const float *__restrict__ state, const __nv_bfloat16 *__restrict__ q,
+                       const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                       const float *__restrict__ alpha, const float *__restrict__ beta,
+                       const uint64_t *__restrict__ anc, int N, int Hk, int Hv, int dk, int dv,
+                       float *__restrict__ out, float *__restrict__ u_out,
+                       float *__restrict__ g_out, const int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (status && status[b] != 0) return;
+  const GdnLayout Ly = gdn_layout(N, dk);
+  const int ks = dk + 4;                                   // padded row stride of S, K, Q
+  float *sS = reinterpret_cast<float *>(smem + Ly.off_s);  // [64][dk + 4]  rows of S_0^T
+  float *sK = reinterpret_cast<float *>(smem + Ly.off_k);  // [N][dk + 4]
+  float *sQ = reinterpret_cast<float *>(smem + Ly.off_q);
+  float *sX = reinterpret_cast<float *>(smem + Ly.off_x);  // [N][N + 1]
+  float *sY = reinterpret_cast<float *>(smem + Ly.off_y);
+  float *sU = reinterpret_cast<float *>(smem + Ly.off_u);  // [N][65]
+  float *sg = reinterpret_cast<float *>(smem + Ly.off_g);
+  float *sal = reinterpret_cast<float *>(smem + Ly.off_al);
+  float *sbe = reinterpret_cast<float *>(smem + Ly.off_be);
+  uint64_t *sanc = reinterpret_cast<uint64_t *>(smem + Ly.off_anc);
+  int *spar = reinterpret_cast<int *>(smem + Ly.off_par);
+  int *sdep = reinterpret_cast<int *>(smem + Ly.off_dep);
+  __shared__ int s_maxdep;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int hk = h / (Hv / Hk);
+  const int j0 = c * kGdnDC + lane;  // this lane's columns: j0 and j0 + 32
+
+  // 1. the 64 rows of S_0^T this CTA owns: asynchronous copies, in flight
+  //    through everything up to the product
+  const float *s0 = state + (((size_t)b * Hv + h) * dv + (size_t)c * kGdnDC) * dk;
+  for (int e = tid * 4; e < kGdnDC * dk; e += kGdnThreads * 4) {
+    const int r = e / dk, i = e - r * dk;
+    cp_async16(sS + r * ks + i, s0 + (size_t)r * dk + i);
+  }
+  // 2. everything else this CTA reads, loads issued before any is used
+  constexpr int kKqIter = kGdnMaxN * 128 / (kGdnThreads * 8);  // at most 4
+  uint4 kw[kKqIter], qw[kKqIter];
+#pragma unroll
+  for (int it = 0; it < kKqIter; ++it) {
+    const int e = (tid + it * kGdnThreads) * 8;
+    if (e < N * dk) {
+      const int t = e / dk, i = e - t * dk;
+      const size_t src = (((size_t)b * N + t) * Hk + hk) * dk + i;
+      kw[it] = *reinterpret_cast<const uint4 *>(k + src);
+      qw[it] = *reinterpret_cast<const uint4 *>(q + src);
+    }
+  }
+  float vpre[ROWS][2];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int t = min(w + kGdnWarps * r, N - 1);
+    const __nv_bfloat16 *vt = v + (((size_t)b * N + t) * Hv + h) * dv + j0;
+    vpre[r][0] = __bfloat162float(vt[0]);
+    vpre[r][1] = __bfloat162float(vt[32]);
+  }
+  if (tid == 0) s_maxdep = 0;
+  for (int t = tid; t < N; t += kGdnThreads) {
+    const uint64_t m = anc[(size_t)b * N + t];
+    sanc[t] = m;
+    sdep[t] = __popcll(m);
+    // the deepest strict ancestor (only bits below t count, so every chain
+    // walked through spar strictly descends and ends)
+    const uint64_t strict = m & ((1ull << t) - 1);
+    spar[t] = strict ? 63 - __clzll((long long)strict) : -1;
+    sal[t] = alpha[((size_t)b * N + t) * Hv + h];
+    sbe[t] = beta[((size_t)b * N + t) * Hv + h];
+  }
+#pragma unroll
+  for (int it = 0; it < kKqIter; ++it) {
+    const int e = (tid + it * kGdnThreads) * 8;
+    if (e < N * dk) {
+      const int t = e / dk, i = e - t * dk;
+      const uint32_t kk[4] = {kw[it].x, kw[it].y, kw[it].z, kw[it].w};
+      const uint32_t qq[4] = {qw[it].x, qw[it].y, qw[it].z, qw[it].w};
+      float4 *dk4 = reinterpret_cast<float4 *>(sK + t * ks + i);
+      float4 *dq4 = reinterpret_cast<float4 *>(sQ + t * ks + i);
+      dk4[0] = make_float4(bf16_lo(kk[0]), bf16_hi(kk[0]), bf16_lo(kk[1]), bf16_hi(kk[1]));
+      dk4[1] = make_float4(bf16_lo(kk[2]), bf16_hi(kk[2]), bf16_lo(kk[3]), bf16_hi(kk[3]));
+      dq4[0] = make_float4(bf16_lo(qq[0]), bf16_hi(qq[0]), bf16_lo(qq[1]), bf16_hi(qq[1]));
+      dq4[1] = make_float4(bf16_lo(qq[2]), bf16_hi(qq[2]), bf16_lo(qq[3]), bf16_hi(qq[3]));
+    }
+  }
+  __syncthreads();
+  // 3. path products g_t (each node walks its own chain) and the deepest level
+  for (int t = tid; t < N; t += kGdnThreads) {
+    float gt = 1.f;
+    for (int i = t; i >= 0; i = spar[i]) gt *= sal[i];
+    sg[t] = gt;
+    atomicMax(&s_maxdep, sdep[t]);
+  }
+  // 4. the ancestor pairs, one thread each: X_ti = beta_t (g_t/g_i) k_t.k_i on
+  //    strict ancestors, Y_ti = (g_t/g_i) q_t.k_i on ancestors-or-self; g_t/g_i
+  //    is the product of alpha over the chain from t up to (not including) i
+  __syncthreads();
+  const int maxdep = s_maxdep;
+  for (int idx = tid; idx < N * maxdep; idx += kGdnThreads) {
+    const int t = idx % N, jup = idx / N;
+    int i = t;
+    float gam = 1.f;
+    for (int s = 0; s < jup && i >= 0; ++s) {
+      gam *= sal[i];
+      i = spar[i];
+    }
+    if (i < 0) continue;  // the chain of t is shorter than jup
+    float kk = 0.f, qk = 0.f;
+    for (int e = 0; e < dk; e += 4) {
+      const float4 a = *reinterpret_cast<const float4 *>(sK + t * ks + e);
+      const float4 qa = *reinterpret_cast<const float4 *>(sQ + t * ks + e);
+      const float4 bb = *reinterpret_cast<const float4 *>(sK + i * ks + e);
+      kk = fmaf(a.x, bb.x, fmaf(a.y, bb.y, fmaf(a.z, bb.z, fmaf(a.w, bb.w, kk))));
+      qk = fmaf(qa.x, bb.x, fmaf(qa.y, bb.y, fmaf(qa.z, bb.z, fmaf(qa.w, bb.w, qk))));
+    }
+    sY[t * (N + 1) + i] = gam * qk;
+    if (jup > 0) sX[t * (N + 1) + i] = sbe[t] * gam * kk;
+  }
+  // 5. K S_0 and Q S_0: warp w owns rows w, w+8, ... (clamped: spare rows
+  //    recompute row N-1 and are dropped), lane l columns l and l+32
+  cp_async_wait_all();
+  __syncthreads();
+  float accp[ROWS][2], accr[ROWS][2];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) accp[r][cc] = accr[r][cc] = 0.f;
+  int trow[ROWS];
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) trow[r] = min(w + kGdnWarps * r, N - 1);
+  for (int i = 0; i < dk; i += 4) {
+    const float4 sa = *reinterpret_cast<const float4 *>(sS + lane * ks + i);
+    const float4 sb = *reinterpret_cast<const float4 *>(sS + (lane + 32) * ks + i);
+    float4 k4[ROWS], q4[ROWS];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      k4[r] = *reinterpret_cast<const float4 *>(sK + trow[r] * ks + i);
+      q4[r] = *reinterpret_cast<const float4 *>(sQ + trow[r] * ks + i);
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+      accp[r][0] = fmaf(k4[r].x, sa.x, fmaf(k4[r].y, sa.y, fmaf(k4[r].z, sa.z, fmaf(k4[r].w, sa.w, accp[r][0]))));
+      accp[r][1] = fmaf(k4[r].x, sb.x, fmaf(k4[r].y, sb.y, fmaf(k4[r].z, sb.z, fmaf(k4[r].w, sb.w, accp[r][1]))));
+      accr[r][0] = fmaf(q4[r].x, sa.x, fmaf(q4[r].y, sa.y, fmaf(q4[r].z, sa.z, fmaf(q4[r].w, sa.w, accr[r][0]))));
+      accr[r][1] = fmaf(q4[r].x, sb.x, fmaf(q4[r].y, sb.y, fmaf(q4[r].z, sb.z, fmaf(q4[r].w, sb.w, accr[r][1]))));
+    }
+  }
+  // 6. right-hand sides beta_t (v_t - g_t (K S_0)_t) into U
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int t = w + kGdnWarps * r;
+    if (t < N) {
+      sU[t * kGdnUStride + lane] = sbe[t] * (vpre[r][0] - sg[t] * accp[r][0]);
+      sU[t * kGdnUStride + lane + 32] = sbe[t] * (vpre[r][1] - sg[t] * accp[r][1]);
+    }
+  }
+  __syncthreads();
+  // 7. forward substitution: warp w owns columns 8w .. 8w+7 of U and every row
+  //    of them (lane l rows l and l+32), so the depth levels only need the warp
+  {
+    const int col0 = 8 * w;
+    for (int d = 2; d <= maxdep; ++d) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int t = lane + 32 * rr;
+        if (t < N && sdep[t] == d) {
+          float x[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) x[cc] = sU[t * kGdnUStride + col0 + cc];
+          for (int i = spar[t]; i >= 0; i = spar[i]) {
+            const float xt = sX[t * (N + 1) + i];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) x[cc] = fmaf(-xt, sU[i * kGdnUStride + col0 + cc], x[cc]);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) sU[t * kGdnUStride + col0 + cc] = x[cc];
+        }
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // 8. outputs o_t = g_t (Q S_0)_t + sum over ancestors-or-self of Y_ti u_i
+#pragma unroll
+  for (int r = 0; r < ROWS; ++r) {
+    const int t = w + kGdnWarps * r;
+    if (t < N) {
+      float o0 = sg[t] * accr[r][0], o1 = sg[t] * accr[r][1];
+      for (int i = t; i >= 0; i = spar[i]) {
+        const float y = sY[t * (N + 1) + i];
+        o0 = fmaf(y, sU[i * kGdnUStride + lane], o0);
+        o1 = fmaf(y, sU[i * kGdnUStride + lane + 32], o1);
+      }
+      const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + j0;
+      out[dst] = o0;
+      out[dst + 32] = o1;
+      u_out[dst] = sU[t * kGdnUStride + lane];
+      u_out[dst + 32] = sU[t * kGdnUStride + lane + 32];
+    }
+  }
+  if (c == 0)
+    for (int t = tid; t < N; t += kGdnThreads) g_out[((size_t)b * N + t) * Hv + h] = sg[t];
+}
+
+constexpr int kGcThreads = 256;
+
+__host__ __device__ inline size_t gc_k_offset(int N) { return ((size_t)N * 8 + 15) / 16 * 16; }
+
+// S_out^T[j][i] = g_l S_0^T[j][i] + sum_p gam_p u_p[j] k_p[i] over the accepted path.
+__global__ void __launch_bounds__(kGcThreads)
+gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__restrict__ k,
+                  const float *__restrict__ u, const float *__restrict__ alpha,
+                  const int32_t *__restrict__ acc_nodes, const int32_t *__restrict__ n_acc, int N,
+                  int Hk, int Hv, int dk, int dv, float *__restrict__ state_out,
+                  const int32_t *__restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / (Hv / Hk);
+  __shared__ int s_len;
+  __shared__ float s_gl;
+  int *spath = reinterpret_cast<int *>(smem);                      // [N]
+  float *sgam = reinterpret_cast<float *>(smem + N * 4);           // [N]
+  float *sku = reinterpret_cast<float *>(smem + gc_k_offset(N));   // [N][dk] k rows, 16-aligned
+  float *suu = sku + (size_t)N * dk;                               // [N][32] u columns
+  if (threadIdx.x == 0) {
+    int L = (status && status[b] != 0) ? 0 : n_acc[b];
+    if (L < 0 || L > N) L = 0;
+    for (int p = 0; p < L; ++p) {
+      const int t = acc_nodes[(size_t)b * N + p];
+      if (t < 0 || t >= N) L = 0;
+      spath[p] = t;
+    }
+    float cur = 1.f;  // product of alpha over the path nodes after p
+    for (int p = L - 1; p >= 0; --p) {
+      sgam[p] = cur;
+      cur *= alpha[((size_t)b * N + spath[p]) * Hv + h];
+    }
+    s_len = L;
+    s_gl = cur;  // g of the last node: the product over the whole path
+  }
+  __syncthreads();
+  const int L = s_len;
+  const float gl = s_gl;
+  for (int e = threadIdx.x; e < L * dk; e += kGcThreads) {
+    const int p = e / dk, i = e - p * dk;
+    sku[e] = __bfloat162float(k[(((size_t)b * N + spath[p]) * Hk + hk) * dk + i]);
+  }
+  for (int e = threadIdx.x; e < L * kGcDC; e += kGcThreads) {
+    const int p = e / kGcDC, jj = e - p * kGcDC;
+    suu[e] = sgam[p] * u[(((size_t)b * N + spath[p]) * Hv + h) * dv + c * kGcDC + jj];
+  }
+  __syncthreads();
+  const size_t base = (((size_t)b * Hv + h) * dv + (size_t)c * kGcDC) * dk;
+  constexpr int kIter = kGcDC * 128 / (kGcThreads * 4);  // at most 4 float4 per thread
+  float4 sv[kIter];
+#pragma unroll
+  for (int it = 0; it < kIter; ++it) {  // every load issued before any is used
+    const int e = (threadIdx.x + it * kGcThreads) * 4;
+    if (e < kGcDC * dk) sv[it] = __ldg(reinterpret_cast<const float4 *>(state_in + base + e));
+  }
+#pragma unroll
+  for (int it = 0; it < kIter; ++it) {
+    const int e = (threadIdx.x + it * kGcThreads) * 4;
+    if (e >= kGcDC * dk) continue;
+    const int jj = e / dk, i = e - jj * dk;
+    float4 s = sv[it];
+    s.x *= gl;
+    s.y *= gl;
+    s.z *= gl;
+    s.w *= gl;
+    for (int p = 0; p < L; ++p) {
+      const float up = suu[p * kGcDC + jj];
+      const float4 k4 = *reinterpret_cast<const float4 *>(sku + (size_t)p * dk + i);
+      s.x = fmaf(up, k4.x, s.x);
+      s.y = fmaf(up, k4.y, s.y);
+      s.z = fmaf(up, k4.z, s.z);
+      s.w = fmaf(up, k4.w, s.w);
+    }
+    *reinterpret_cast<float4 *>(state_out + base + e) = s;
+  }
+}
+
+bool gdn_shape_ok(int B, int N, int Hk, int Hv, int dk, int dv) {
+  return B >= 0 && N >= 1 && N <= kGdnMaxN && Hk >= 1 && Hv >= 1 && Hv % Hk == 0 && dk >= 32 &&
+         dk <= 128 && dk % 32 == 0 && dv >= 64 && dv <= 128 && dv % 64 == 0;
+}
+
+}  // namespace
+}  // namespace tv
+
+using namespace tv;
+
+extern "C" tv_status tv_gdn_tree_verify(const float *state, const void *q, const void *k,
+                                        const void *v, const float *alpha, const float *beta,
+                                        const uint64_t *anc, int B, int N, int Hk, int Hv, int dk,
+                                        int dv, float *out, float *u, float *g,
+                                        const int32_t *status, tv_stream stream) {
+  if (!gdn_shape_ok(B, N, Hk, Hv, dk, dv)) return TV_ERR_ARG;
+  if (B == 0) return TV_OK;
+  if (!state || !q || !k || !v || !alpha || !beta || !anc || !out || !u || !g) return TV_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(q) |
+       reinterpret_cast<uintptr_t>(k)) & 15)
+    return TV_ERR_ARG;
+  const GdnLayout Ly = gdn_layout(N, dk);
+  const dim3 grid(dv / kGdnDC, Hv, B);
+  auto kern = N <= 32 ? gdn_tree_verify_kernel<4> : gdn_tree_verify_kernel<8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly.bytes) !=
+      cudaSuccess)
+    return TV_ERR_CUDA;
+  kern<<<grid, kGdnThreads, Ly.bytes, as_stream(stream)>>>(
+      state, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+      static_cast<const __nv_bfloat16 *>(v), alpha, beta, anc, N, Hk, Hv, dk, dv, out, u, g, status);
+  return launch_status();
+}
+
+extern "C" tv_status tv_gdn_commit(const float *state_in, const void *k, const float *u,
+                                   const float *alpha, const int32_t *acc_nodes,
+                                   const int32_t *n_acc, int B, int N, int Hk, int Hv, int dk,
+                                   int dv, float *state_out, const int32_t *status,
+                                   tv_stream stream) {
+  if (!gdn_shape_ok(B, N, Hk, Hv, dk, dv)) return TV_ERR_ARG;
+  if (B == 0) return TV_OK;
+  if (!state_in || !k || !u || !alpha || !acc_nodes || !n_acc || !state_out) return TV_ERR_ARG;
+  if (state_in == state_out) return TV_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(state_in) | reinterpret_cast<uintptr_t>(state_out)) & 15)
+    return TV_ERR_ARG;
+  const size_t smem = gc_k_offset(N) + (size_t)N * dk * 4 + (size_t)N * kGcDC * 4;
+  if (cudaFuncSetAttribute(gdn_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return TV_ERR_CUDA;
+  const dim3 grid(dv / kGcDC, Hv, B);
+  gdn_commit_kernel<<<grid, kGcThreads, smem, as_stream(stream)>>>(
+      state_in, static_cast<const __nv_bfloat16 *>(k), u, alpha, acc_nodes, n_acc, N, Hk, Hv, dk,
+      dv, state_out, status);
+  return launch_status();
+}

@@ -506,3 +506,66 @@ def make_layers(inp, num_layers: int, seed: int):
         layers.append({k: _randn_bf16(tuple(inp[k].shape), gen, dev)
                        for k in ("q", "k_tree", "v_tree", "k_cache", "v_cache")})
     return layers
+
+
+# --------------------------------------------------------------------------- GDN layers
+
+@dataclasses.dataclass(frozen=True)
+class GdnWorkload:
+    """Tree verification through one Gated DeltaNet layer."""
+    name: str
+    seed: int
+    B: int
+    N: int
+    max_depth: int
+    Hk: int       # query / key heads
+    Hv: int       # value heads (state heads)
+    dk: int
+    dv: int
+
+
+GDN_WORKLOADS = {
+    # the stress batch and trees through a GDN layer of 16 key / 32 value heads, 128 x 128 state
+    "gdn_stress": GdnWorkload("gdn_stress", 3000, 64, 32, 8, 16, 32, 128, 128),
+    "gdn_small": GdnWorkload("gdn_small", 3001, 3, 12, 5, 2, 4, 32, 64),
+}
+
+
+def make_gdn(name, device="cpu", seed: Optional[int] = None, *, B=None, N=None, tree=None,
+             Hk=None, Hv=None, dk=None, dv=None):
+    """Seeded inputs of one GDN tree verification: tree (parent, depth),
+    L2-normalised q / k (bf16, as GDN layers normalise them), v ~ N(0, 1) bf16,
+    decay alpha ~ U(0.8, 1), write strength beta = sigmoid(N(0, 1)), committed
+    state S_0 ~ N(0, 0.3^2) fp32 stored transposed [B, Hv, dv, dk]."""
+    w = GDN_WORKLOADS[name]
+    seed = w.seed if seed is None else seed
+    B = w.B if B is None else B
+    N = w.N if N is None else N
+    Hk = w.Hk if Hk is None else Hk
+    Hv = w.Hv if Hv is None else Hv
+    dk = w.dk if dk is None else dk
+    dv = w.dv if dv is None else dv
+    rng = np.random.Generator(np.random.PCG64(seed))
+    parent = np.zeros((B, N), np.int32)
+    for b in range(B):
+        if tree == "chain":
+            parent[b] = tree_chain(N)
+        elif tree == "star":
+            parent[b] = tree_star(N)
+        else:
+            parent[b] = tree_random(rng, N, w.max_depth)
+    depth = np.stack([depths_of(parent[b]) for b in range(B)])
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    q = torch.randn(B, N, Hk, dk, generator=gen, device=dev)
+    k = torch.randn(B, N, Hk, dk, generator=gen, device=dev)
+    q = (q / q.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    k = (k / k.norm(dim=-1, keepdim=True)).to(torch.bfloat16)
+    v = torch.randn(B, N, Hv, dv, generator=gen, device=dev).to(torch.bfloat16)
+    alpha = 0.8 + 0.2 * torch.rand(B, N, Hv, generator=gen, device=dev)
+    beta = torch.sigmoid(torch.randn(B, N, Hv, generator=gen, device=dev))
+    state = 0.3 * torch.randn(B, Hv, dv, dk, generator=gen, device=dev)
+    it = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+    return dict(B=B, N=N, Hk=Hk, Hv=Hv, dk=dk, dv=dv, parent=it(parent), depth=it(depth),
+                q=q, k=k, v=v, alpha=alpha.float(), beta=beta.float(), state=state.float())
