@@ -42,15 +42,24 @@ extern "C" {
  *   out     float32 [B, N, Hv, dv]   o_t = S_t^T q_t
  *   u       float32 [B, N, Hv, dv]   pseudo-values, kept for tv_gdn_commit
  *   g       float32 [B, N, Hv]       product of alpha along each node's path
+ *   kernel  0 auto, 1 CUDA cores (fp32 FMA), 2 tensor cores (tcgen05; d_k 64
+ *           or 128).  Auto takes the tensor cores where they apply.  On the
+ *           tensor cores K and Q enter as the bf16 they are and the fp32 state
+ *           as three bf16 planes (hi + mid + lo, 24 significant bits), with
+ *           fp32 accumulation: both kernels give fp32-accurate products.
  *   status  int32   [B]              sequences with a non-zero status (a
  *                                    malformed tree) are skipped: their outputs
- *                                    are left untouched
- * Errors: TV_ERR_ARG (NULL pointers, sizes out of range).
+ *                                    are left untouched; a wait of the
+ *                                    tensor-core kernel that runs past its
+ *                                    bound (never on a healthy GPU) writes
+ *                                    TV_ERR_CUDA
+ * Errors: TV_ERR_ARG (NULL pointers, sizes out of range), TV_ERR_UNSUPPORTED
+ * (kernel 2 with d_k not 64 or 128).
  */
 tv_status tv_gdn_tree_verify(const float *state, const void *q, const void *k, const void *v,
                              const float *alpha, const float *beta, const uint64_t *anc, int B,
                              int N, int Hk, int Hv, int dk, int dv, float *out, float *u, float *g,
-                             const int32_t *status, tv_stream stream);
+                             int kernel, int32_t *status, tv_stream stream);
 
 /*
  * tv_gdn_commit -- the state after the accepted path acc_nodes[b][0 .. n_acc[b]):

@@ -43,7 +43,7 @@ def oracle_inputs(x):
                 alpha=f(x["alpha"]), beta=f(x["beta"]), anc=anc)
 
 
-def run_verify(tv, x):
+def run_verify(tv, x, kernel=0):
     B, N, Hv, dv = x["B"], x["N"], x["Hv"], x["dv"]
     anc = torch.empty(B, N, dtype=torch.int64, device="cuda")
     pos = torch.empty(B, N, dtype=torch.int32, device="cuda")
@@ -54,7 +54,7 @@ def run_verify(tv, x):
     u = torch.full((B, N, Hv, dv), float("nan"), device="cuda")
     g = torch.full((B, N, Hv), float("nan"), device="cuda")
     tv.tv_gdn_tree_verify(x["state"], x["q"], x["k"], x["v"], x["alpha"], x["beta"], anc, out, u,
-                          g, st)
+                          g, st, kernel=kernel)
     torch.cuda.synchronize()
     return out, u, g, st
 
@@ -66,19 +66,23 @@ def close(got, ref):
     assert err.max() <= 0, f"max excess {err.max():.3e}"
 
 
-CASES = [
+CASES = [  # d_k 64 / 128 run on the tensor cores under kernel 0, the rest on CUDA cores
     dict(),                                                       # gdn_small: dk 32, dv 64
     dict(B=2, N=32, Hk=4, Hv=8, dk=128, dv=128),                  # the stress head shape
     dict(B=2, N=64, Hk=1, Hv=2, dk=96, dv=64, tree="chain"),      # depth 64
+    dict(B=2, N=64, Hk=2, Hv=4, dk=64, dv=128, tree="chain"),     # depth 64, 2N = 128 rows
     dict(B=2, N=40, Hk=2, Hv=2, dk=128, dv=64, tree="star"),      # depth 1 everywhere
+    dict(B=3, N=45, Hk=1, Hv=3, dk=128, dv=64),                   # K and Q rows across TMEM quadrants
     dict(B=1, N=1, Hk=1, Hv=1, dk=32, dv=64),                     # a single node
+    dict(B=1, N=1, Hk=1, Hv=1, dk=64, dv=64),
 ]
 
 
+@pytest.mark.parametrize("kernel", [0, 1])
 @pytest.mark.parametrize("kw", CASES)
-def test_verify_matches_oracle(tv, kw):
+def test_verify_matches_oracle(tv, kw, kernel):
     x = to_dev(workloads.make_gdn("gdn_small", "cpu", **kw))
-    out, u, g, _ = run_verify(tv, x)
+    out, u, g, _ = run_verify(tv, x, kernel)
     o = oracle_inputs(x)
     ref = ogdn.tree_verify(o["state"], o["q"], o["k"], o["v"], o["alpha"], o["beta"], o["anc"])
     close(out, ref["out"])
@@ -86,11 +90,12 @@ def test_verify_matches_oracle(tv, kw):
     close(g, ref["g"])
 
 
-def test_verify_full_size_sampled(tv):
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_verify_full_size_sampled(tv, kernel):
     """The gdn_stress workload (64 sequences x 32 value heads, 128 x 128 state):
     every output computed, four (sequence, head) pairs checked in full."""
     x = to_dev(workloads.make_gdn("gdn_stress", "cpu"))
-    out, u, g, _ = run_verify(tv, x)
+    out, u, g, _ = run_verify(tv, x, kernel)
     for b, h in ((0, 0), (17, 5), (40, 31), (63, 16)):
         hk = h // (x["Hv"] // x["Hk"])
         sub = dict(x, B=1, Hk=1, Hv=1, parent=x["parent"][b:b + 1], depth=x["depth"][b:b + 1],
@@ -133,3 +138,14 @@ def test_commit_matches_oracle(tv, kw):
     ref = ogdn.commit(o["state"], o["k"], o["v"], o["alpha"], o["beta"], acc, n_acc)
     close(new, np.swapaxes(ref, -1, -2))
     assert torch.equal(new[B - 1], x["state"][B - 1])  # empty accept copies S_0 bit for bit
+
+
+def test_tensor_and_cuda_cores_agree(tv):
+    """Both kernels on the same full-size inputs: every output within the
+    tolerance of each other (each is within it of the fp64 oracle)."""
+    x = to_dev(workloads.make_gdn("gdn_stress", "cpu", B=16))
+    o1, u1, g1, _ = run_verify(tv, x, 1)
+    o2, u2, g2, _ = run_verify(tv, x, 2)
+    close(o2, o1.double().cpu().numpy())
+    close(u2, u1.double().cpu().numpy())
+    assert torch.equal(g1, g2)

@@ -127,7 +127,7 @@ def _load():
     lib.tv_verify_graph_launches.restype = I
     lib.tv_verify_graph_destroy.argtypes = [P]
     lib.tv_verify_graph_destroy.restype = None
-    lib.tv_gdn_tree_verify.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, P, P]
+    lib.tv_gdn_tree_verify.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, P]
     lib.tv_gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
               "tv_commit_kv", "tv_topk", "tv_build_tree", "tv_verify_step",
@@ -394,7 +394,8 @@ def tv_verify_graph_destroy(graph):
     lib.tv_verify_graph_destroy(graph)
 
 
-def tv_gdn_tree_verify(state, q, k, v, alpha, beta, anc, out, u, g, status=None, stream=None):
+def tv_gdn_tree_verify(state, q, k, v, alpha, beta, anc, out, u, g, status=None, kernel=0,
+                       stream=None):
     """GDN outputs of every tree node from the committed state (include/tv_gdn.h).
     state float32 [B, Hv, dv, dk] (S^T); q, k bf16 [B, N, Hk, dk]; v bf16
     [B, N, Hv, dv]; alpha, beta float32 [B, N, Hv]; anc int64 [B, N]."""
@@ -405,7 +406,8 @@ def tv_gdn_tree_verify(state, q, k, v, alpha, beta, anc, out, u, g, status=None,
         _ptr(state, f32, "state"), _ptr(q, bf16, "q"), _ptr(k, bf16, "k"), _ptr(v, bf16, "v"),
         _ptr(alpha, f32, "alpha"), _ptr(beta, f32, "beta"), _ptr(anc, torch.int64, "anc"),
         B, N, Hk, Hv, dk, dv, _ptr(out, f32, "out"), _ptr(u, f32, "u"), _ptr(g, f32, "g"),
-        _ptr(status, torch.int32, "status") if status is not None else None, _stream(stream)))
+        int(kernel), _ptr(status, torch.int32, "status") if status is not None else None,
+        _stream(stream)))
 
 
 def tv_gdn_commit(state_in, k, u, alpha, acc_nodes, n_acc, state_out, status=None, stream=None):

@@ -27,6 +27,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 #include "tv_gdn.h"
 
 namespace tv {
@@ -37,6 +38,13 @@ constexpr int kGcDC = 32;      // rows of S^T per commit CTA
 constexpr int kGdnWarps = 8;
 constexpr int kGdnThreads = 32 * kGdnWarps;
 constexpr int kGdnMaxN = 64;
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.b32 %0, 1, 0, e;\n\t}"
+               : "=r"(p));
+  return p != 0;
+}
 
 // 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all)
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
@@ -283,6 +291,334 @@ gdn_tree_verify_kernel(const float *__restrict__ state, const __nv_bfloat16 *__r
     for (int t = tid; t < N; t += kGdnThreads) g_out[((size_t)b * N + t) * Hv + h] = sg[t];
 }
 
+// ------------------------------------------------------------------ tensor cores
+//
+// d_k in {64, 128}: [K; Q] S_0 on tcgen05.  A = the 2N rows of K and Q (bf16,
+// exactly the inputs), B = the 64 state rows split into three bf16 planes
+// (hi + mid + lo reproduces the fp32 value to 24 bits), D = 128 x 64 fp32 in
+// TMEM, accumulated over the planes.  Both operands are K-major with the
+// 128-byte swizzle, written here by the threads (every 16-byte chunk is one
+// swizzle unit).  One elected thread issues the 3 * d_k / 16 MMAs and commits
+// them to an mbarrier; the CUDA cores work out g, X and Y meanwhile.  Every
+// wait is bounded (2 s); on expiry status[b] = TV_ERR_CUDA.
+
+constexpr int kTcM = 128;
+constexpr int kTcCols = 64;  // TMEM columns: one fp32 column per d_v column
+constexpr unsigned long long kGdnWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t gdn_sw128_desc(uint32_t addr) {
+  // start >> 4, leading offset 16 B, stride 1024 B between 8-row groups,
+  // descriptor version 1, 128-byte swizzle
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)(16 >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// kind::f16 instruction descriptor: fp32 D, bf16 A and B, both K-major
+__host__ __device__ constexpr uint32_t gdn_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+// byte offset of 16-byte chunk ch (0..7) of row r in a [rows][64] bf16 half tile
+__device__ __forceinline__ uint32_t swz(int r, int ch) {
+  return (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
+}
+
+__device__ __forceinline__ uint64_t gdn_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __noinline__ bool gdn_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = gdn_timer();
+  for (uint32_t i = 0;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && gdn_timer() - t0 > kGdnWaitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return a | (b << 16);
+}
+
+struct GdnTcLayout {
+  size_t off_a, off_b, off_x, off_y, off_u, off_g, off_al, off_be, off_anc, off_par, off_dep,
+      bytes;
+};
+
+__host__ __device__ inline GdnTcLayout gdn_tc_layout(int N, int dk) {
+  GdnTcLayout L;
+  const int halves = dk / 64;
+  size_t o = 0;
+  L.off_a = o; o += (size_t)halves * kTcM * 128;       // [halves][128][64] bf16
+  L.off_b = o; o += (size_t)3 * halves * kTcCols * 128; // [3 planes][halves][64][64] bf16
+  L.off_x = o; o += (size_t)N * (N + 1) * 4;
+  L.off_y = o; o += (size_t)N * (N + 1) * 4;
+  L.off_u = o; o += (size_t)N * kGdnUStride * 4;
+  L.off_g = o; o += (size_t)N * 4;
+  L.off_al = o; o += (size_t)N * 4;
+  L.off_be = o; o += (size_t)N * 4;
+  o = (o + 7) / 8 * 8;
+  L.off_anc = o; o += (size_t)N * 8;
+  L.off_par = o; o += (size_t)N * 4;
+  L.off_dep = o; o += (size_t)N * 4;
+  L.bytes = o + 1024;  // slack: the tile base is rounded up to 1024 B
+  return L;
+}
+
+__global__ void __launch_bounds__(kGdnThreads)
+gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *__restrict__ q,
+                          const __nv_bfloat16 *__restrict__ k, const __nv_bfloat16 *__restrict__ v,
+                          const float *__restrict__ alpha, const float *__restrict__ beta,
+                          const uint64_t *__restrict__ anc, int N, int Hk, int Hv, int dk, int dv,
+                          float *__restrict__ out, float *__restrict__ u_out,
+                          float *__restrict__ g_out, int32_t *__restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ __align__(8) unsigned long long s_bar;
+  __shared__ int s_maxdep;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  if (status && status[b] != 0) return;
+  const GdnTcLayout Ly = gdn_tc_layout(N, dk);
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  unsigned char *smem = smem_raw + (((raw + 1023) & ~1023u) - raw);
+  unsigned char *sA = smem + Ly.off_a;
+  unsigned char *sB = smem + Ly.off_b;
+  float *sX = reinterpret_cast<float *>(smem + Ly.off_x);  // [N][N + 1]
+  float *sY = reinterpret_cast<float *>(smem + Ly.off_y);
+  float *sU = reinterpret_cast<float *>(smem + Ly.off_u);  // [N][65]
+  float *sg = reinterpret_cast<float *>(smem + Ly.off_g);
+  float *sal = reinterpret_cast<float *>(smem + Ly.off_al);
+  float *sbe = reinterpret_cast<float *>(smem + Ly.off_be);
+  uint64_t *sanc = reinterpret_cast<uint64_t *>(smem + Ly.off_anc);
+  int *spar = reinterpret_cast<int *>(smem + Ly.off_par);
+  int *sdep = reinterpret_cast<int *>(smem + Ly.off_dep);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int hk = h / (Hv / Hk);
+  const int halves = dk / 64;
+  const uint32_t half_a = kTcM * 128, half_b = kTcCols * 128, plane_b = halves * half_b;
+
+  if (w == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(&s_tmem), kTcCols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 32) {
+    ptx::mbar_init(ptx::smem_u32(&s_bar), 1);
+    ptx::fence_mbar_init();
+    s_maxdep = 0;
+  }
+  // 1. loads, all issued before use: K / Q chunks, the state rows, v of this
+  //    thread's right-hand-side row
+  const int nkq = 2 * N * dk / 8;                 // 16-byte chunks of K and Q
+  constexpr int kKqIt = 2 * kGdnMaxN * 128 / 8 / kGdnThreads;  // at most 8
+  uint4 kq[kKqIt];
+#pragma unroll
+  for (int it = 0; it < kKqIt; ++it) {
+    const int e = tid + it * kGdnThreads;
+    if (e < nkq) {
+      const int isq = e >= N * dk / 8, rem = isq ? e - N * dk / 8 : e;
+      const int t = rem / (dk / 8), i = (rem - t * (dk / 8)) * 8;
+      const __nv_bfloat16 *src = (isq ? q : k) + (((size_t)b * N + t) * Hk + hk) * dk + i;
+      kq[it] = *reinterpret_cast<const uint4 *>(src);
+    }
+  }
+  const float *s0 = state + (((size_t)b * Hv + h) * dv + (size_t)c * kTcCols) * dk;
+  constexpr int kSIt = kTcCols * 128 / 8 / kGdnThreads;  // chunks of 8 per thread: at most 4
+  float4 sv[kSIt][2];
+#pragma unroll
+  for (int it = 0; it < kSIt; ++it) {
+    const int e = (tid + it * kGdnThreads) * 8;
+    if (e < kTcCols * dk) {
+      sv[it][0] = __ldg(reinterpret_cast<const float4 *>(s0 + e));
+      sv[it][1] = __ldg(reinterpret_cast<const float4 *>(s0 + e + 4));
+    }
+  }
+  const int quad = w & 3, chalf = w >> 2;  // TMEM lane quadrant, 32-column half
+  const int drow = 32 * quad + lane;       // the D row this thread reads
+  uint4 vq[4];
+  if (drow < N) {
+    const uint4 *vs = reinterpret_cast<const uint4 *>(
+        v + (((size_t)b * N + drow) * Hv + h) * dv + (size_t)c * kTcCols + 32 * chalf);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) vq[p] = vs[p];
+  }
+  for (int t = tid; t < N; t += kGdnThreads) {
+    const uint64_t m = anc[(size_t)b * N + t];
+    sanc[t] = m;
+    sdep[t] = __popcll(m);
+    const uint64_t strict = m & ((1ull << t) - 1);
+    spar[t] = strict ? 63 - __clzll((long long)strict) : -1;
+    sal[t] = alpha[((size_t)b * N + t) * Hv + h];
+    sbe[t] = beta[((size_t)b * N + t) * Hv + h];
+  }
+  // 2. operands into the swizzled tiles
+#pragma unroll
+  for (int it = 0; it < kKqIt; ++it) {
+    const int e = tid + it * kGdnThreads;
+    if (e < nkq) {
+      const int isq = e >= N * dk / 8, rem = isq ? e - N * dk / 8 : e;
+      const int t = rem / (dk / 8), i = (rem - t * (dk / 8)) * 8;
+      const int row = isq ? N + t : t;
+      *reinterpret_cast<uint4 *>(sA + (i >> 6) * half_a + swz(row, (i & 63) >> 3)) = kq[it];
+    }
+  }
+#pragma unroll
+  for (int it = 0; it < kSIt; ++it) {
+    const int e = (tid + it * kGdnThreads) * 8;
+    if (e < kTcCols * dk) {
+      const int r = e / dk, i = e - r * dk;
+      const float x[8] = {sv[it][0].x, sv[it][0].y, sv[it][0].z, sv[it][0].w,
+                          sv[it][1].x, sv[it][1].y, sv[it][1].z, sv[it][1].w};
+      float hi[8], mid[8], lo[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        hi[p] = __bfloat162float(__float2bfloat16_rn(x[p]));
+        const float r1 = x[p] - hi[p];
+        mid[p] = __bfloat162float(__float2bfloat16_rn(r1));
+        lo[p] = r1 - mid[p];
+      }
+      const uint32_t off = (i >> 6) * half_b + swz(r, (i & 63) >> 3);
+      *reinterpret_cast<uint4 *>(sB + off) =
+          make_uint4(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]),
+                     pack_bf16x2(hi[4], hi[5]), pack_bf16x2(hi[6], hi[7]));
+      *reinterpret_cast<uint4 *>(sB + plane_b + off) =
+          make_uint4(pack_bf16x2(mid[0], mid[1]), pack_bf16x2(mid[2], mid[3]),
+                     pack_bf16x2(mid[4], mid[5]), pack_bf16x2(mid[6], mid[7]));
+      *reinterpret_cast<uint4 *>(sB + 2 * plane_b + off) =
+          make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                     pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+    }
+  }
+  ptx::fence_proxy_async_smem();  // the tiles are read by the tensor cores next
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t bar = ptx::smem_u32(&s_bar);
+  // 3. the MMAs: one elected thread
+  if (w == 0) {
+    if (elect_one()) {
+      const uint32_t a0 = ptx::smem_u32(sA), b0 = ptx::smem_u32(sB);
+      const uint32_t idesc = gdn_idesc(kTcM, kTcCols);
+      for (int p = 0; p < 3; ++p)
+        for (int kk = 0; kk < dk / 16; ++kk) {
+          const uint32_t in = (kk >> 2), ks = (kk & 3) * 32;
+          const uint64_t ad = gdn_sw128_desc(a0 + in * half_a + ks);
+          const uint64_t bd = gdn_sw128_desc(b0 + p * plane_b + in * half_b + ks);
+          ptx::umma_f16(tmem, ad, bd, idesc, (p | kk) != 0);
+        }
+      ptx::umma_commit(bar);
+    }
+    __syncwarp();
+  }
+  // 4. meanwhile: path products, then the ancestor pairs from the bf16 tile
+  for (int t = tid; t < N; t += kGdnThreads) {
+    float gt = 1.f;
+    for (int i = t; i >= 0; i = spar[i]) gt *= sal[i];
+    sg[t] = gt;
+    atomicMax(&s_maxdep, sdep[t]);
+  }
+  __syncthreads();
+  const int maxdep = s_maxdep;
+  for (int idx = tid; idx < N * maxdep; idx += kGdnThreads) {
+    const int t = idx % N, jup = idx / N;
+    int i = t;
+    float gam = 1.f;
+    for (int s2 = 0; s2 < jup && i >= 0; ++s2) {
+      gam *= sal[i];
+      i = spar[i];
+    }
+    if (i < 0) continue;
+    float kk = 0.f, qk = 0.f;
+    for (int hf = 0; hf < halves; ++hf)
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(sA + hf * half_a + swz(t, ch));
+        const uint4 qa = *reinterpret_cast<const uint4 *>(sA + hf * half_a + swz(N + t, ch));
+        const uint4 bb = *reinterpret_cast<const uint4 *>(sA + hf * half_a + swz(i, ch));
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, qw[4] = {qa.x, qa.y, qa.z, qa.w},
+                       bw[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          kk = fmaf(bf16_lo(aw[p]), bf16_lo(bw[p]), fmaf(bf16_hi(aw[p]), bf16_hi(bw[p]), kk));
+          qk = fmaf(bf16_lo(qw[p]), bf16_lo(bw[p]), fmaf(bf16_hi(qw[p]), bf16_hi(bw[p]), qk));
+        }
+      }
+    sY[t * (N + 1) + i] = gam * qk;
+    if (jup > 0) sX[t * (N + 1) + i] = sbe[t] * gam * kk;
+  }
+  // 5. the product: D row d (K row d, or Q row d - N), 32 columns per warp
+  bool ok = gdn_wait(bar, 0);
+  if (!ok) ok = gdn_wait(bar, 0);  // a second bounded chance before TMEM is freed
+  ptx::tc_fence_after();
+  uint32_t dv32[32];
+  ptx::tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + 32 * chalf, dv32);
+  ptx::tmem_wait_ld();
+  if (!ok && tid == 0) set_status(status, b, TV_ERR_CUDA);
+  // 6. right-hand sides beta_t (v_t - g_t (K S_0)_t) into U
+  if (drow < N) {
+    const int t = drow;
+    const float bt = sbe[t], gt = sg[t];
+    const uint32_t vw[16] = {vq[0].x, vq[0].y, vq[0].z, vq[0].w, vq[1].x, vq[1].y, vq[1].z, vq[1].w,
+                             vq[2].x, vq[2].y, vq[2].z, vq[2].w, vq[3].x, vq[3].y, vq[3].z, vq[3].w};
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const float vv = (jj & 1) ? bf16_hi(vw[jj >> 1]) : bf16_lo(vw[jj >> 1]);
+      sU[t * kGdnUStride + 32 * chalf + jj] = bt * (vv - gt * __uint_as_float(dv32[jj]));
+    }
+  }
+  __syncthreads();
+  // 7. forward substitution (warp w: columns 8w .. 8w+7, every row)
+  {
+    const int col0 = 8 * w;
+    for (int d = 2; d <= maxdep; ++d) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int t = lane + 32 * rr;
+        if (t < N && sdep[t] == d) {
+          float x[8];
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) x[cc] = sU[t * kGdnUStride + col0 + cc];
+          for (int i = spar[t]; i >= 0; i = spar[i]) {
+            const float xt = sX[t * (N + 1) + i];
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) x[cc] = fmaf(-xt, sU[i * kGdnUStride + col0 + cc], x[cc]);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) sU[t * kGdnUStride + col0 + cc] = x[cc];
+        }
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // 8. outputs from the Q rows: o_t = g_t (Q S_0)_t + sum over ancestors-or-self of Y_ti u_i
+  if (drow >= N && drow < 2 * N) {
+    const int t = drow - N;
+    const float gt = sg[t];
+    float o[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) o[jj] = gt * __uint_as_float(dv32[jj]);
+    for (int i = t; i >= 0; i = spar[i]) {
+      const float y = sY[t * (N + 1) + i];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(y, sU[i * kGdnUStride + 32 * chalf + jj], o[jj]);
+    }
+    const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + (size_t)c * kTcCols + 32 * chalf;
+#pragma unroll
+    for (int jj = 0; jj < 32; jj += 4) {
+      *reinterpret_cast<float4 *>(out + dst + jj) = make_float4(o[jj], o[jj + 1], o[jj + 2], o[jj + 3]);
+      const float *us = sU + t * kGdnUStride + 32 * chalf + jj;
+      *reinterpret_cast<float4 *>(u_out + dst + jj) = make_float4(us[0], us[1], us[2], us[3]);
+    }
+  }
+  if (c == 0)
+    for (int t = tid; t < N; t += kGdnThreads) g_out[((size_t)b * N + t) * Hv + h] = sg[t];
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (w == 0) ptx::tmem_dealloc(tmem, kTcCols);
+}
+
 constexpr int kGcThreads = 256;
 
 __host__ __device__ inline size_t gc_k_offset(int N) { return ((size_t)N * 8 + 15) / 16 * 16; }
@@ -374,23 +710,38 @@ using namespace tv;
 extern "C" tv_status tv_gdn_tree_verify(const float *state, const void *q, const void *k,
                                         const void *v, const float *alpha, const float *beta,
                                         const uint64_t *anc, int B, int N, int Hk, int Hv, int dk,
-                                        int dv, float *out, float *u, float *g,
-                                        const int32_t *status, tv_stream stream) {
+                                        int dv, float *out, float *u, float *g, int kernel,
+                                        int32_t *status, tv_stream stream) {
   if (!gdn_shape_ok(B, N, Hk, Hv, dk, dv)) return TV_ERR_ARG;
+  if (kernel < 0 || kernel > 2) return TV_ERR_ARG;
+  const bool tc_ok = dk == 64 || dk == 128;
+  if (kernel == 2 && !tc_ok) return TV_ERR_UNSUPPORTED;
   if (B == 0) return TV_OK;
   if (!state || !q || !k || !v || !alpha || !beta || !anc || !out || !u || !g) return TV_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(q) |
-       reinterpret_cast<uintptr_t>(k)) & 15)
+       reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(u)) & 15)
     return TV_ERR_ARG;
-  const GdnLayout Ly = gdn_layout(N, dk);
   const dim3 grid(dv / kGdnDC, Hv, B);
+  const auto *qb = static_cast<const __nv_bfloat16 *>(q);
+  const auto *kb = static_cast<const __nv_bfloat16 *>(k);
+  const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+  if (tc_ok && kernel != 1) {
+    const GdnTcLayout Ly = gdn_tc_layout(N, dk);
+    if (cudaFuncSetAttribute(gdn_tree_verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)Ly.bytes) != cudaSuccess)
+      return TV_ERR_CUDA;
+    gdn_tree_verify_tc_kernel<<<grid, kGdnThreads, Ly.bytes, as_stream(stream)>>>(
+        state, qb, kb, vb, alpha, beta, anc, N, Hk, Hv, dk, dv, out, u, g, status);
+    return launch_status();
+  }
+  const GdnLayout Ly = gdn_layout(N, dk);
   auto kern = N <= 32 ? gdn_tree_verify_kernel<4> : gdn_tree_verify_kernel<8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly.bytes) !=
       cudaSuccess)
     return TV_ERR_CUDA;
-  kern<<<grid, kGdnThreads, Ly.bytes, as_stream(stream)>>>(
-      state, static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-      static_cast<const __nv_bfloat16 *>(v), alpha, beta, anc, N, Hk, Hv, dk, dv, out, u, g, status);
+  kern<<<grid, kGdnThreads, Ly.bytes, as_stream(stream)>>>(state, qb, kb, vb, alpha, beta, anc, N,
+                                                          Hk, Hv, dk, dv, out, u, g, status);
   return launch_status();
 }
 
