@@ -675,6 +675,34 @@ def measure_gdn(name, steps, warmup, dev, batch=None, seed_offset=0):
     }
 
 
+def gdn_cpu_baseline(name, budget_s=10.0):
+    """The oracle (fp64 per-path recurrence) on a bounded sample of the GDN
+    workload: whole (sequence, value head) problems until the budget is spent,
+    scaled to the full step."""
+    import numpy as np
+    import workloads
+    from oracle import gdn as ogdn
+    import oracle
+    w = workloads.GDN_WORKLOADS[name]
+    oracle.build()
+    done, spent = 0, 0.0
+    while spent < budget_s and done < w.B * w.Hv:
+        x = workloads.make_gdn(name, "cpu", seed=w.seed + 7919 * (done + 1), B=1, Hk=1, Hv=1)
+        mask, _, _ = oracle.ancestors(x["parent"].numpy(), x["depth"].numpy(),
+                                      np.full(1, 10, np.int32))
+        anc = (mask.astype(np.uint64) << np.arange(mask.shape[2], dtype=np.uint64)).sum(-1)
+        f = lambda t: t.double().numpy()
+        st = np.swapaxes(f(x["state"]), -1, -2)
+        t0 = time.perf_counter()
+        ogdn.tree_verify(st, f(x["q"]), f(x["k"]), f(x["v"]), f(x["alpha"]), f(x["beta"]), anc)
+        spent += time.perf_counter() - t0
+        done += 1
+    per_step = spent / done * w.B * w.Hv
+    return {"value": 1.0 / per_step, "unit": "steps/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {w.B * w.Hv} (sequence, value head) problems of {name} "
+                      f"(numpy fp64 per-path recurrence), scaled by {w.B * w.Hv}/{done}"}
+
+
 def bench_gdn(args, rank, world, local):
     import torch
     torch.cuda.set_device(local)
@@ -697,6 +725,8 @@ def bench_gdn(args, rank, world, local):
                      "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 flop x SM clock"},
         "verify_ms": r["verify_ms"], "commit_ms": r["commit_ms"], "commit_gbs": r["commit_gbs"],
         "gpu_launches": 2 * args.steps, "status_ok": r["status_ok"],
+        **({"cpu_baseline": gdn_cpu_baseline("gdn_stress")}
+           if not args.no_cpu_baseline and world == 1 else {}),
     }
 
 

@@ -342,8 +342,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 struct GdnTcLayout {
-  size_t off_a, off_b, off_x, off_y, off_u, off_g, off_al, off_be, off_anc, off_par, off_dep,
-      bytes;
+  size_t off_a, off_b, off_x, off_y, off_u, off_r, off_g, off_al, off_be, off_anc, off_par,
+      off_dep, bytes;
 };
 
 __host__ __device__ inline GdnTcLayout gdn_tc_layout(int N, int dk) {
@@ -355,6 +355,7 @@ __host__ __device__ inline GdnTcLayout gdn_tc_layout(int N, int dk) {
   L.off_x = o; o += (size_t)N * (N + 1) * 4;
   L.off_y = o; o += (size_t)N * (N + 1) * 4;
   L.off_u = o; o += (size_t)N * kGdnUStride * 4;
+  L.off_r = o; o += (size_t)N * kGdnUStride * 4;        // Q S_0 rows, staged from TMEM
   L.off_g = o; o += (size_t)N * 4;
   L.off_al = o; o += (size_t)N * 4;
   L.off_be = o; o += (size_t)N * 4;
@@ -387,6 +388,7 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
   float *sX = reinterpret_cast<float *>(smem + Ly.off_x);  // [N][N + 1]
   float *sY = reinterpret_cast<float *>(smem + Ly.off_y);
   float *sU = reinterpret_cast<float *>(smem + Ly.off_u);  // [N][65]
+  float *sR = reinterpret_cast<float *>(smem + Ly.off_r);  // [N][65]
   float *sg = reinterpret_cast<float *>(smem + Ly.off_g);
   float *sal = reinterpret_cast<float *>(smem + Ly.off_al);
   float *sbe = reinterpret_cast<float *>(smem + Ly.off_be);
@@ -566,6 +568,9 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
       const float vv = (jj & 1) ? bf16_hi(vw[jj >> 1]) : bf16_lo(vw[jj >> 1]);
       sU[t * kGdnUStride + 32 * chalf + jj] = bt * (vv - gt * __uint_as_float(dv32[jj]));
     }
+  } else if (drow < 2 * N) {  // a Q row: stage (Q S_0)_t for the output phase
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) sR[(drow - N) * kGdnUStride + 32 * chalf + jj] = __uint_as_float(dv32[jj]);
   }
   __syncthreads();
   // 7. forward substitution (warp w: columns 8w .. 8w+7, every row)
@@ -592,25 +597,21 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
     }
   }
   __syncthreads();
-  // 8. outputs from the Q rows: o_t = g_t (Q S_0)_t + sum over ancestors-or-self of Y_ti u_i
-  if (drow >= N && drow < 2 * N) {
-    const int t = drow - N;
+  // 8. outputs o_t = g_t (Q S_0)_t + sum over ancestors-or-self of Y_ti u_i:
+  //    warp w rows w, w+8, ...; lane l columns l and l+32 (coalesced writes)
+  for (int t = w; t < N; t += kGdnWarps) {
     const float gt = sg[t];
-    float o[32];
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) o[jj] = gt * __uint_as_float(dv32[jj]);
+    float o0 = gt * sR[t * kGdnUStride + lane], o1 = gt * sR[t * kGdnUStride + lane + 32];
     for (int i = t; i >= 0; i = spar[i]) {
       const float y = sY[t * (N + 1) + i];
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) o[jj] = fmaf(y, sU[i * kGdnUStride + 32 * chalf + jj], o[jj]);
+      o0 = fmaf(y, sU[i * kGdnUStride + lane], o0);
+      o1 = fmaf(y, sU[i * kGdnUStride + lane + 32], o1);
     }
-    const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + (size_t)c * kTcCols + 32 * chalf;
-#pragma unroll
-    for (int jj = 0; jj < 32; jj += 4) {
-      *reinterpret_cast<float4 *>(out + dst + jj) = make_float4(o[jj], o[jj + 1], o[jj + 2], o[jj + 3]);
-      const float *us = sU + t * kGdnUStride + 32 * chalf + jj;
-      *reinterpret_cast<float4 *>(u_out + dst + jj) = make_float4(us[0], us[1], us[2], us[3]);
-    }
+    const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + (size_t)c * kTcCols + lane;
+    out[dst] = o0;
+    out[dst + 32] = o1;
+    u_out[dst] = sU[t * kGdnUStride + lane];
+    u_out[dst + 32] = sU[t * kGdnUStride + lane + 32];
   }
   if (c == 0)
     for (int t = tid; t < N; t += kGdnThreads) g_out[((size_t)b * N + t) * Hv + h] = sg[t];
