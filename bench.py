@@ -16,6 +16,7 @@ own batch, no collective touches the data path (weak scaling).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -52,6 +53,8 @@ def parse():
                          "gdn: tree verification through a Gated DeltaNet layer + state commit")
     ap.add_argument("--layers", type=int, default=8, help="attention layers for --path graph")
     ap.add_argument("--draft-workload", default="tree_build")
+    ap.add_argument("--window-left", type=int, default=None,
+                    help="override the workload's sliding window (-1: global attention)")
     return ap.parse_args()
 
 
@@ -181,11 +184,13 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def workload_config(name, B=None):
+def workload_config(name, B=None, window_left=None):
     """The workload, described from its specification (both arms use this)."""
     import workloads
     w = workloads.get(name)
     B = w.B if B is None else B
+    if window_left is not None:
+        w = dataclasses.replace(w, window_left=window_left)
     ctx = f"{w.ctx[0]}..{w.ctx[1]}" if isinstance(w.ctx, tuple) else str(w.ctx)
     return {
         "workload": (f"{name}: B={B} ctx={ctx} N={w.N} Hq/Hkv/D={w.Hq}/{w.Hkv}/{w.D} bf16 KV, "
@@ -217,7 +222,8 @@ def bench_ours(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    inp = workloads.make(args.workload, dev, seed=rank_seed(args.workload, rank), B=args.batch)
+    inp = workloads.make(args.workload, dev, seed=rank_seed(args.workload, rank), B=args.batch,
+                         window_left=args.window_left)
     step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
                          inp["max_blocks"], window_left=inp["window_left"],
                          logits_dtype=inp["logits_dtype"], device=dev)
@@ -328,7 +334,7 @@ def bench_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "impl": "ours",
-        "config": workload_config(args.workload, args.batch),
+        "config": workload_config(args.workload, args.batch, args.window_left),
         "attention": {"ms": attn_ms, "kv_gbs": achieved, "algorithmic_bytes": alg,
                       "frac_of_8tbs_nominal": achieved / 8000.0,
                       "frac_of_peak": achieved / peak, "peak_kind": peak_kind},
@@ -349,11 +355,12 @@ def bench_ours(args, rank, world, local):
         # the multi-layer step as one CUDA-graph replay, on the small best-first batch
         line["graph_path"] = measure_graph("best_first", 8, 50, 3, dev)
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0)
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0,
+                                            window_left=args.window_left)
     return line
 
 
-def cpu_baseline(name, budget_s=12.0, seqs_max=None):
+def cpu_baseline(name, budget_s=12.0, seqs_max=None, window_left=None):
     """The oracle, as it stands, on a bounded sample: whole verify steps for a
     few sequences at a time (all heads, all nodes), until the time budget is
     spent; scaled to whole-batch steps/s."""
@@ -368,7 +375,7 @@ def cpu_baseline(name, budget_s=12.0, seqs_max=None):
     seqs_max = B if seqs_max is None else seqs_max
     b = 0
     while done < seqs_max and spent < budget_s:
-        inp = workloads.make(name, "cpu", seed=w.seed + 7919 * (b + 1), B=1)
+        inp = workloads.make(name, "cpu", seed=w.seed + 7919 * (b + 1), B=1, window_left=window_left)
         npi = workloads.to_numpy(inp)
         t = time.perf_counter()
         oracle.verify_step(npi)
