@@ -725,11 +725,14 @@ def bench_gdn(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "impl": "ours", "path": "gdn",
         "config": {"workload": r["workload"], "l2": "state 134 MB read per step"},
-        "roofline": {"kernel": "tv_gdn_tree_verify", "bound": "alu",
-                     "achieved": r["verify_tflops"], "peak": r["fp32_peak_tflops"],
-                     "unit": "TFLOP/s", "frac": r["verify_tflops"] / r["fp32_peak_tflops"],
-                     "traffic": None,
-                     "peak_source": "152 SMs x 128 fp32 FMA lanes x 2 flop x SM clock"},
+        # the product runs on the tensor cores, so the kernel's bound is HBM:
+        # the state, q / k / v and the outputs it must move once per step
+        "roofline": {"kernel": "tv_gdn_tree_verify", "bound": "hbm",
+                     "achieved": r["verify_bytes"] / (r["verify_ms"] * 1e-3) / 1e9,
+                     "peak": peaks()[0], "unit": "GB/s",
+                     "frac": r["verify_bytes"] / (r["verify_ms"] * 1e-3) / 1e9 / peaks()[0],
+                     "traffic": None, "peak_source": peaks()[1]},
+        "verify_fp32_tflops": r["verify_tflops"],
         "verify_ms": r["verify_ms"], "commit_ms": r["commit_ms"], "commit_gbs": r["commit_gbs"],
         "gpu_launches": 2 * args.steps, "status_ok": r["status_ok"],
         **({"cpu_baseline": gdn_cpu_baseline("gdn_stress")}
