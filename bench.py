@@ -348,6 +348,8 @@ def bench_ours(args, rank, world, local):
         "clocks": clocks,
     }
     if world == 1:
+        # the same step with tv_argmax on 16 SMs beside the attention (two streams)
+        line["overlapped_step"] = measure_overlap(args.workload, inp, min(K, 300), dev)
         # the draft-tree path (the step before verify), timed on its own
         d = measure_draft("tree_build", 50, 3, dev)
         d.pop("_inputs")
@@ -358,6 +360,31 @@ def bench_ours(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=12.0,
                                             window_left=args.window_left)
     return line
+
+
+def measure_overlap(name, inp, steps, dev, argmax_sms=16):
+    """The verify step with tv_argmax_sm on `argmax_sms` SMs of a second stream
+    beside tv_tree_attention on the others (VerifyStep(argmax_sms=...)):
+    CUDA events on the main stream around `steps` steps."""
+    import torch
+    import tree_speculative_decoding_build_gb300 as tv
+    step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
+                         inp["max_blocks"], window_left=inp["window_left"],
+                         logits_dtype=inp["logits_dtype"], device=dev, argmax_sms=argmax_sms)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(5):
+        step(inp)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step(inp)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    return {"argmax_sms": argmax_sms, "ms_per_step": ms, "steps_per_s": 1000.0 / ms,
+            "status_ok": bool((step.out.status == 0).all().item())}
 
 
 def cpu_baseline(name, budget_s=12.0, seqs_max=None, window_left=None):

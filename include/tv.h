@@ -116,6 +116,11 @@ tv_status tv_build_ancestors(const int32_t *parent, const int32_t *depth,
  *              cores), 1 = CUDA-core kernel, 2 = tensor-core kernel
  *              (TV_ERR_UNSUPPORTED outside its shapes: D = 128,
  *              (Hq/Hkv)*N <= 128, B <= 1024)
+ *   max_ctas   at most this many persistent CTAs for the tensor-core kernel,
+ *              one per SM (0 = every SM).  Leaving SMs free lets another
+ *              kernel that does not depend on this one, such as tv_argmax_sm
+ *              on a second stream, run beside it.  Ignored by the CUDA-core
+ *              kernel.
  *   out        bf16 [B, N, Hq, D]         softmax(scale q.K^T) V per node and head
  *   status     int32 [B]                  TV_ERR_BLOCK is recorded when a needed
  *                                         block id is outside [0, num_blocks) or
@@ -145,6 +150,7 @@ typedef struct tv_attn_args {
   float sm_scale;
   int num_splits;
   int kernel;
+  int max_ctas;
   void *out;
   int32_t *status;
 } tv_attn_args;
@@ -194,6 +200,18 @@ size_t tv_argmax_workspace_size(int64_t rows, int64_t V, int dtype);
 tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
                     int64_t row_stride, int32_t *out_idx, void *workspace,
                     size_t workspace_bytes, tv_stream stream);
+
+/*
+ * tv_argmax_sm -- tv_argmax with its streaming plan held to at most sm_limit
+ * SMs (one CTA each; 0 = every SM), so that it can run beside a kernel that
+ * occupies the other SMs, e.g. tv_tree_attention with max_ctas = SMs -
+ * sm_limit on another stream: the two read HBM at the same time.  The chunk
+ * plan ignores the limit.  Same arguments, workspace, result and errors as
+ * tv_argmax otherwise (tv_argmax_workspace_size covers every limit).
+ */
+tv_status tv_argmax_sm(const void *logits, int dtype, int64_t rows, int64_t V,
+                       int64_t row_stride, int32_t *out_idx, void *workspace,
+                       size_t workspace_bytes, int sm_limit, tv_stream stream);
 
 /*
  * tv_argmax_noalloc -- tv_argmax for callers that cannot allocate device memory.

@@ -442,3 +442,32 @@ def test_whole_step_full_size_stress(tv):
     keep = ~touched
     assert torch.equal(inp["k_cache"].transpose(1, 2)[keep], kc0.transpose(1, 2)[keep])
     assert np.array_equal(o.ctx_len_out.cpu().numpy(), ctx + n_acc)
+
+
+# ------------------------------------------------------------------ SM partitioning
+
+def test_attention_with_fewer_ctas_and_overlapped_argmax(tv):
+    """tv_tree_attention with max_ctas < SMs (the tensor-core kernel cuts its
+    work into fewer ranges) stays within tolerance of the oracle, and the step
+    that runs tv_argmax_sm beside it gives the same argmax, tokens and commits."""
+    inp = workloads.make("best_first", "cuda", B=3, plant="path")
+    seq = step_for(inp)
+    lap = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
+                        inp["max_blocks"], window_left=inp["window_left"],
+                        logits_dtype=inp["logits_dtype"], argmax_sms=16)
+    k0, v0 = inp["k_cache"].clone(), inp["v_cache"].clone()
+    a = seq(inp)
+    torch.cuda.synchronize()
+    ref = {k: getattr(a, k).clone() for k in ("argmax", "out_tokens", "n_acc", "ctx_len_out", "attn")}
+    kc1 = inp["k_cache"].clone()
+    inp["k_cache"].copy_(k0)
+    inp["v_cache"].copy_(v0)
+    b = lap(inp)
+    torch.cuda.synchronize()
+    for k in ("argmax", "out_tokens", "n_acc", "ctx_len_out"):
+        assert torch.equal(getattr(b, k), ref[k]), k
+    assert torch.equal(inp["k_cache"], kc1)
+    npi = workloads.to_numpy(dict(inp, k_cache=k0, v_cache=v0))
+    exp = oracle_attention(npi)
+    assert_close(b.attn.float().cpu().numpy(), exp)
+    assert_close(ref["attn"].float().cpu().numpy(), exp)

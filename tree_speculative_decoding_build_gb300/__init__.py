@@ -53,11 +53,23 @@ class StepOutputs:
 
 
 class VerifyStep:
-    """One verify step for a fixed batch shape; buffers are allocated once."""
+    """One verify step for a fixed batch shape; buffers are allocated once.
+
+    ``argmax_sms`` > 0 runs tv_argmax beside tv_tree_attention instead of after
+    it: the argmax goes to a second stream holding ``argmax_sms`` SMs
+    (tv_argmax_sm), the attention keeps the rest (max_ctas), and the walk waits
+    for both.  The two HBM-bound kernels then read memory at the same time."""
 
     def __init__(self, B, N, Hq, Hkv, D, V, max_blocks, window_left=-1, logits_dtype="bf16",
-                 num_splits=0, device="cuda"):
+                 num_splits=0, device="cuda", argmax_sms=0):
         dev = torch.device(device)
+        self.argmax_sms = int(argmax_sms)
+        if self.argmax_sms > 0:
+            self.side = torch.cuda.Stream(device=dev)
+            self.ev_fork = torch.cuda.Event()
+            self.ev_join = torch.cuda.Event()
+            sms = torch.cuda.get_device_properties(dev).multi_processor_count
+            self.attn_ctas = max(1, sms - self.argmax_sms)
         i32 = torch.int32
         self.shape = dict(B=B, N=N, Hq=Hq, Hkv=Hkv, D=D, V=V, max_blocks=max_blocks)
         self.window_left = window_left
@@ -85,13 +97,24 @@ class VerifyStep:
         """Enqueue the whole step for ``inp`` (dict of device tensors)."""
         o = self.out
         B, N = inp["tokens"].shape
+        main = stream if stream is not None else torch.cuda.current_stream()
+        if self.argmax_sms > 0:  # the argmax on its own SMs, beside the attention
+            self.ev_fork.record(main)
+            self.side.wait_event(self.ev_fork)
+            tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), self.ws_arg, self.side,
+                      sm_limit=self.argmax_sms)
+            self.ev_join.record(self.side)
         tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], o.anc, o.pos, o.status,
                            stream)
         tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
                           inp["block_table"], inp["ctx_len"], o.pos, o.anc, o.attn, o.status,
                           window_left=self.window_left, num_splits=self.num_splits,
-                          workspace=self.ws_attn, stream=stream)
-        tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), self.ws_arg, stream)
+                          workspace=self.ws_attn, stream=stream,
+                          max_ctas=self.attn_ctas if self.argmax_sms > 0 else 0)
+        if self.argmax_sms > 0:
+            main.wait_event(self.ev_join)
+        else:
+            tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), self.ws_arg, stream)
         tv_tree_walk(inp["tokens"], inp["parent"], o.argmax, inp["root_pred"], o.status,
                      o.out_tokens, o.n_emit, o.acc_nodes, o.n_acc, stream)
         tv_commit_kv(inp["k_tree"], inp["v_tree"], o.acc_nodes, o.n_acc, inp["ctx_len"],

@@ -33,6 +33,7 @@ EXPORTS = (
     "tv_tree_attention",
     "tv_argmax_workspace_size",
     "tv_argmax",
+    "tv_argmax_sm",
     "tv_argmax_noalloc",
     "tv_tree_walk",
     "tv_commit_kv",
@@ -66,7 +67,7 @@ class AttnArgs(ctypes.Structure):
         ("D", ctypes.c_int), ("block_size", ctypes.c_int), ("max_blocks", ctypes.c_int),
         ("num_blocks", ctypes.c_int), ("window_left", ctypes.c_int), ("window_right", ctypes.c_int),
         ("sm_scale", ctypes.c_float), ("num_splits", ctypes.c_int), ("kernel", ctypes.c_int),
-        ("out", ctypes.c_void_p), ("status", ctypes.c_void_p),
+        ("max_ctas", ctypes.c_int), ("out", ctypes.c_void_p), ("status", ctypes.c_void_p),
     ]
 
 
@@ -112,6 +113,8 @@ def _load():
     lib.tv_argmax_workspace_size.argtypes = [L, L, I]
     lib.tv_argmax_workspace_size.restype = S
     lib.tv_argmax.argtypes = [P, I, L, L, L, P, P, S, P]
+    lib.tv_argmax_sm.argtypes = [P, I, L, L, L, P, P, S, I, P]
+    lib.tv_argmax_sm.restype = I
     lib.tv_argmax_noalloc.argtypes = [P, I, L, L, L, P, P]
     lib.tv_argmax_noalloc.restype = I
     lib.tv_tree_walk.argtypes = [P, P, P, P, P, I, I, P, P, P, P, P]
@@ -181,7 +184,7 @@ KERNEL_AUTO, KERNEL_CUDA_CORE, KERNEL_TENSOR_CORE = 0, 1, 2
 
 
 def attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
-              window_left=-1, window_right=0, sm_scale=0.0, num_splits=0, kernel=0):
+              window_left=-1, window_right=0, sm_scale=0.0, num_splits=0, kernel=0, max_ctas=0):
     bf = torch.bfloat16
     B, N, Hq, D = q.shape
     a = AttnArgs()
@@ -203,6 +206,7 @@ def attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, an
     a.sm_scale = float(sm_scale)
     a.num_splits = int(num_splits)
     a.kernel = int(kernel)
+    a.max_ctas = int(max_ctas)
     a.out = _ptr(out, bf, "out")
     a.status = _ptr(status, torch.int32, "status")
     return a
@@ -223,9 +227,9 @@ def tv_tree_attention_workspace_size(B, N, Hq, Hkv, D, max_blocks, window_left=-
 
 def tv_tree_attention(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out,
                       status, window_left=-1, window_right=0, sm_scale=0.0, num_splits=0,
-                      workspace=None, stream=None, kernel=0):
+                      workspace=None, stream=None, kernel=0, max_ctas=0):
     a = attn_args(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_len, pos, anc, out, status,
-                  window_left, window_right, sm_scale, num_splits, kernel)
+                  window_left, window_right, sm_scale, num_splits, kernel, max_ctas)
     need = int(lib.tv_tree_attention_workspace_size(ctypes.byref(a)))
     if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -246,8 +250,9 @@ def _logits_dtype(t):
     raise TypeError(f"logits: unsupported dtype {t.dtype}")
 
 
-def tv_argmax(logits, out_idx, workspace=None, stream=None):
-    """Row argmax of a 2-D ``logits`` [rows, V] (rows may be strided)."""
+def tv_argmax(logits, out_idx, workspace=None, stream=None, sm_limit=None):
+    """Row argmax of a 2-D ``logits`` [rows, V] (rows may be strided).  With
+    ``sm_limit`` the streaming plan uses at most that many SMs (tv_argmax_sm)."""
     if logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits: expected a 2-D tensor with unit inner stride")
     if not logits.is_cuda:
@@ -259,6 +264,11 @@ def tv_argmax(logits, out_idx, workspace=None, stream=None):
         workspace = torch.empty(need, dtype=torch.uint8, device=logits.device)
     wp = _ptr(workspace, None, "workspace") if workspace is not None else None
     wb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if sm_limit is not None:
+        _check("tv_argmax_sm", lib.tv_argmax_sm(
+            ctypes.c_void_p(logits.data_ptr()), dt, rows, V, logits.stride(0),
+            _ptr(out_idx, torch.int32, "out_idx"), wp, wb, int(sm_limit), _stream(stream)))
+        return
     _check("tv_argmax", lib.tv_argmax(ctypes.c_void_p(logits.data_ptr()), dt, rows, V,
                                       logits.stride(0), _ptr(out_idx, torch.int32, "out_idx"),
                                       wp, wb, _stream(stream)))

@@ -380,10 +380,10 @@ ArgmaxPlan chunk_plan(long long rows, long long V, int esize) {
 }
 
 ArgmaxPlan plan_argmax(const void *logits, long long rows, long long V, long long row_stride,
-                       int esize) {
+                       int esize, int sm_limit = 0) {
   if (stream_shape(rows, V, esize) && row_stride == V &&
       (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
-    const int ctas = sm_count();
+    const int ctas = sm_limit > 0 && sm_limit < sm_count() ? sm_limit : sm_count();
     return ArgmaxPlan{true, 1, 0, ctas, (size_t)2 * ctas * kStrWarps};
   }
   return chunk_plan(rows, V, esize);
@@ -458,13 +458,14 @@ extern "C" size_t tv_argmax_workspace_size(int64_t rows, int64_t V, int dtype) {
   return ((n * sizeof(float) + 255) / 256) * 256 + n * sizeof(int32_t);
 }
 
-extern "C" tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
-                               int64_t row_stride, int32_t *out_idx, void *workspace,
-                               size_t workspace_bytes, tv_stream stream) {
+extern "C" tv_status tv_argmax_sm(const void *logits, int dtype, int64_t rows, int64_t V,
+                                  int64_t row_stride, int32_t *out_idx, void *workspace,
+                                  size_t workspace_bytes, int sm_limit, tv_stream stream) {
+  if (sm_limit < 0) return TV_ERR_ARG;
   const tv_status st = check_args(logits, dtype, rows, V, row_stride, out_idx);
   if (st != TV_OK || rows == 0) return st;
   const int esize = dtype == TV_F32 ? 4 : 2;
-  const ArgmaxPlan p = plan_argmax(logits, rows, V, row_stride, esize);
+  const ArgmaxPlan p = plan_argmax(logits, rows, V, row_stride, esize, sm_limit);
   if (!p.stream && (long long)rows * p.chunks > (long long)INT32_MAX) return TV_ERR_ARG;
   float *pv = nullptr;
   int32_t *pi = nullptr;
@@ -477,6 +478,13 @@ extern "C" tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int6
                                      ((n * sizeof(float) + 255) / 256) * 256);
   }
   return launch_argmax(logits, dtype, rows, V, row_stride, out_idx, p, pv, pi, as_stream(stream));
+}
+
+extern "C" tv_status tv_argmax(const void *logits, int dtype, int64_t rows, int64_t V,
+                               int64_t row_stride, int32_t *out_idx, void *workspace,
+                               size_t workspace_bytes, tv_stream stream) {
+  return tv_argmax_sm(logits, dtype, rows, V, row_stride, out_idx, workspace, workspace_bytes, 0,
+                      stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -28,6 +28,7 @@ struct AttnParams {
   float2 *part_ml;       // [B*Hkv][splits][R]     (running max, running sum)
   __nv_bfloat16 *out;    // [B, N, Hq, D]
   int32_t *status;       // [B]
+  int ctas;              // tensor-core kernel: persistent CTAs (0 = one per SM)
 };
 
 // First visible context block of a sequence: rows sit at positions

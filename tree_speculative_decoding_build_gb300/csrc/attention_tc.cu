@@ -968,7 +968,7 @@ size_t attention_tc_workspace(int B, int P) {
 }
 
 cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream_t stream) {
-  const int P = sm_count();
+  const int P = a.ctas > 0 && a.ctas < sm_count() ? a.ctas : sm_count();
   TcParams tp{};
   tp.a = a;
   char *ws = static_cast<char *>(workspace);
