@@ -253,45 +253,71 @@ attn_generic_kernel(const AttnParams p) {
 
 // One warp per output row: O = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
 __global__ void attn_combine_kernel(const AttnParams p) {
+  // One warp per output row.  The split maxima and weights are formed by the
+  // lanes in parallel (lane j holds split c*32 + j of each chunk of 32); the
+  // weighted sum walks the splits four at a time so their loads overlap.
+  // Lane l owns dims 8l .. 8l+7 (D <= 256).
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.Hkv * p.R;
   if (row >= rows) return;
   const int bk = (int)(row / p.R), r = (int)(row - (long long)bk * p.R);
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
-  float M = -INFINITY;
-  for (int s = 0; s < p.splits; ++s)
-    M = fmaxf(M, p.part_ml[((size_t)bk * p.splits + s) * p.R + r].x);
   const int D = p.D;
-  const int t = r / p.G, g = r - t * p.G;
-  __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * D;
+  const size_t pr0 = (size_t)bk * p.splits * p.R + r;  // partial row of split s: pr0 + s * R
+  float M = -INFINITY;
+  for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_ml[pr0 + (size_t)s * p.R].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f;
   float acc[8];
-  for (int d0 = 0; d0 < D; d0 += 256) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    L = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-      const size_t pr = ((size_t)bk * p.splits + s) * p.R + r;
-      const float2 ml = p.part_ml[pr];
-      if (ml.x == -INFINITY) continue;
-      const float w = exp2f(ml.x - M);
-      L += ml.y * w;
-      const float *src = p.part_o + pr * D + d0 + lane * 8;
-      if (d0 + lane * 8 < D) {
-        const float4 a = *reinterpret_cast<const float4 *>(src);
-        const float4 c = *reinterpret_cast<const float4 *>(src + 4);
-        acc[0] += a.x * w; acc[1] += a.y * w; acc[2] += a.z * w; acc[3] += a.w * w;
-        acc[4] += c.x * w; acc[5] += c.y * w; acc[6] += c.z * w; acc[7] += c.w * w;
+  for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+  const bool mine = lane * 8 < D;
+  for (int c0 = 0; c0 < p.splits; c0 += 32) {
+    // this chunk's weights, one split per lane
+    const int sl = c0 + lane;
+    float wl = 0.f;
+    if (sl < p.splits) {
+      const float2 ml = p.part_ml[pr0 + (size_t)sl * p.R];
+      if (ml.x != -INFINITY) {
+        wl = exp2f(ml.x - M);
+        L += ml.y * wl;
       }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    if (d0 + lane * 8 < D) {
-      __nv_bfloat16 *o = dst + d0 + lane * 8;
+    const int n = min(32, p.splits - c0);
+    for (int j = 0; j < n; j += 4) {
+      float4 va[4], vb[4];
+      float w[4];
 #pragma unroll
-      for (int e = 0; e < 8; e += 2)
-        *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+      for (int u = 0; u < 4; ++u) {
+        w[u] = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
+        if (j + u < n && w[u] != 0.f && mine) {
+          const float *src = p.part_o + (pr0 + (size_t)(c0 + j + u) * p.R) * D + lane * 8;
+          va[u] = *reinterpret_cast<const float4 *>(src);
+          vb[u] = *reinterpret_cast<const float4 *>(src + 4);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (j + u < n && w[u] != 0.f && mine) {
+          acc[0] += va[u].x * w[u]; acc[1] += va[u].y * w[u];
+          acc[2] += va[u].z * w[u]; acc[3] += va[u].w * w[u];
+          acc[4] += vb[u].x * w[u]; acc[5] += vb[u].y * w[u];
+          acc[6] += vb[u].z * w[u]; acc[7] += vb[u].w * w[u];
+        }
+      }
     }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  if (mine) {
+    const int t = r / p.G, g = r - t * p.G;
+    __nv_bfloat16 *o = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * D + lane * 8;
+#pragma unroll
+    for (int e = 0; e < 8; e += 2)
+      *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
   }
 }
 

@@ -417,16 +417,36 @@ __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
   const long long c0 = p - 1;
   const long long xl = rs + vpr - 1;              // owner of the row's last vector:
   const long long c1 = ((xl + 1) * owners + nv - 1) / nv - 1;  // ceil((x+1)*owners/nv) - 1
-  float lv = -INFINITY;
-  int li = INT32_MAX;
-  for (long long c = c0; c <= c1; ++c) {
-    const long long s0 = ts_split(c, nv, owners);
-    if (s0 == ts_split(c + 1, nv, owners)) continue;  // empty range
-    const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
-    for (int j = 0; j < k; ++j) {
-      const int xi = part_i[slot * k + j];
-      if (xi == INT32_MAX) break;
-      wl_insert(lv, li, part_v[slot * k + j], xi);
+  // the pieces' lists, 32 candidates per step, one per lane; only candidates
+  // that beat the current k-th entry are inserted (a ballot hands them over)
+  float lv = -INFINITY, tv = -INFINITY;
+  int li = INT32_MAX, ti = INT32_MAX;
+  const long long total = (c1 - c0 + 1) * k;
+  for (long long q0 = 0; q0 < total; q0 += 32) {
+    const long long qq = q0 + lane;
+    float x = -INFINITY;
+    int xi = INT32_MAX;
+    if (qq < total) {
+      const long long c = c0 + qq / k;
+      const int jj = (int)(qq - (qq / k) * k);
+      const long long s0 = ts_split(c, nv, owners);
+      if (s0 != ts_split(c + 1, nv, owners)) {  // empty ranges wrote nothing
+        const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
+        x = part_v[slot * k + jj];
+        xi = part_i[slot * k + jj];
+      }
+    }
+    unsigned ballot = __ballot_sync(0xffffffffu, xi != INT32_MAX && beats(x, xi, tv, ti));
+    while (ballot) {
+      const int src = __ffs(ballot) - 1;
+      ballot &= ballot - 1;
+      const float y = __shfl_sync(0xffffffffu, x, src);
+      const int yi = __shfl_sync(0xffffffffu, xi, src);
+      if (beats(y, yi, tv, ti)) {
+        wl_insert(lv, li, y, yi);
+        tv = __shfl_sync(0xffffffffu, lv, k - 1);
+        ti = __shfl_sync(0xffffffffu, li, k - 1);
+      }
     }
   }
   if (lane < k) {
