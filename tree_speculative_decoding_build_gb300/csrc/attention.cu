@@ -25,8 +25,11 @@ namespace tv {
 namespace {
 
 constexpr int kCcThreads = 256;
-constexpr int kCcRows = 64;          // rows per thread block
-constexpr int kCcRowsPerWarp = kCcRows / (kCcThreads / 32);
+// rows per thread block: 64, or 32 at D = 256 (the output accumulators of 8
+// rows x 8 dims per lane would take every register and leave one CTA per SM)
+template <int D>
+constexpr int cc_rows() { return D >= 256 ? 32 : 64; }
+constexpr int kCcRowsMax = 64;
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem, bool valid) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -42,8 +45,10 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // a warp computes 16 dot products per row with one shuffle to join halves.
 // In the P.V phase lane l owns output dims [l*D/32, (l+1)*D/32).
 template <int D>
-__global__ void __launch_bounds__(kCcThreads)
+__global__ void __launch_bounds__(kCcThreads, D >= 256 ? 2 : 1)
 attn_generic_kernel(const AttnParams p) {
+  constexpr int kCcRows = cc_rows<D>();
+  constexpr int kCcRowsPerWarp = kCcRows / (kCcThreads / 32);
   constexpr int KP = D + 16;         // padded K row: consecutive keys 32 bytes apart mod 128
   constexpr int DL = D / 32;         // output dims per lane
   constexpr int NG = D / 16;         // 8-dim groups per lane in the score phase
@@ -152,32 +157,49 @@ attn_generic_kernel(const AttnParams p) {
     const int key = is_node ? (i - n_ctx_tiles) * 16 + kk : (t_begin + i) * kBlock + kk;
     const bool key_ok = s_tile_ok[st] && (is_node ? key < p.N : key < ctx);
     const int key_pos = is_node ? (key_ok ? s_npos[key] : 0) : key;
-    uint4 kf[NG];
     const __nv_bfloat16 *krow = k_s + st * 16 * KP + kk * KP;
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi)
-      kf[gi] = *reinterpret_cast<const uint4 *>(krow + (2 * gi + hh) * 8);
     const __nv_bfloat16 *vt = v_s + st * 16 * D + lane * DL;
+    // scores of this warp's rows against key kk, in chunks of at most 8
+    // 16-byte K fragments so that no more than 8 are live at once
+    constexpr int NGC = NG < 8 ? NG : 8;
+    float sc[kCcRowsPerWarp][2];
+#pragma unroll
+    for (int j = 0; j < kCcRowsPerWarp; ++j) sc[j][0] = sc[j][1] = 0.f;
+#pragma unroll
+    for (int g0 = 0; g0 < NG; g0 += NGC) {
+      uint4 kf[NGC];
+#pragma unroll
+      for (int gi = 0; gi < NGC; ++gi)
+        kf[gi] = *reinterpret_cast<const uint4 *>(krow + (2 * (g0 + gi) + hh) * 8);
+#pragma unroll
+      for (int j = 0; j < kCcRowsPerWarp; ++j) {
+        const int rr = warp + j * (kCcThreads / 32);
+        if (rr >= nrows) break;                         // warp-uniform
+        const float *qr = q_s + rr * D;
+        float s0 = sc[j][0], s1 = sc[j][1];
+#pragma unroll
+        for (int gi = 0; gi < NGC; ++gi) {
+          const float4 qa = *reinterpret_cast<const float4 *>(qr + (2 * (g0 + gi) + hh) * 8);
+          const float4 qb = *reinterpret_cast<const float4 *>(qr + (2 * (g0 + gi) + hh) * 8 + 4);
+          const uint4 kw = kf[gi];
+          s0 = fmaf(qa.x, bf16_lo(kw.x), s0);
+          s1 = fmaf(qa.y, bf16_hi(kw.x), s1);
+          s0 = fmaf(qa.z, bf16_lo(kw.y), s0);
+          s1 = fmaf(qa.w, bf16_hi(kw.y), s1);
+          s0 = fmaf(qb.x, bf16_lo(kw.z), s0);
+          s1 = fmaf(qb.y, bf16_hi(kw.z), s1);
+          s0 = fmaf(qb.z, bf16_lo(kw.w), s0);
+          s1 = fmaf(qb.w, bf16_hi(kw.w), s1);
+        }
+        sc[j][0] = s0;
+        sc[j][1] = s1;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < kCcRowsPerWarp; ++j) {
       const int rr = warp + j * (kCcThreads / 32);
       if (rr >= nrows) break;                         // warp-uniform
-      const float *qr = q_s + rr * D;
-      float s = 0.f;
-#pragma unroll
-      for (int gi = 0; gi < NG; ++gi) {
-        const float4 qa = *reinterpret_cast<const float4 *>(qr + (2 * gi + hh) * 8);
-        const float4 qb = *reinterpret_cast<const float4 *>(qr + (2 * gi + hh) * 8 + 4);
-        const uint4 kw = kf[gi];
-        s = fmaf(qa.x, bf16_lo(kw.x), s);
-        s = fmaf(qa.y, bf16_hi(kw.x), s);
-        s = fmaf(qa.z, bf16_lo(kw.y), s);
-        s = fmaf(qa.w, bf16_hi(kw.y), s);
-        s = fmaf(qb.x, bf16_lo(kw.z), s);
-        s = fmaf(qb.y, bf16_hi(kw.z), s);
-        s = fmaf(qb.z, bf16_lo(kw.w), s);
-        s = fmaf(qb.w, bf16_hi(kw.w), s);
-      }
+      float s = sc[j][0] + sc[j][1];
       s += __shfl_xor_sync(0xffffffffu, s, 1);
       const int rpos = s_rpos[rr];
       bool ok = key_ok;
@@ -323,6 +345,7 @@ __global__ void attn_combine_kernel(const AttnParams p) {
 
 template <int D>
 void launch_generic_d(const AttnParams &p, cudaStream_t stream) {
+  constexpr int kCcRows = cc_rows<D>();
   const size_t smem = (size_t)kCcRows * D * sizeof(float) +
                       (size_t)2 * 16 * (D + 16) * sizeof(__nv_bfloat16) +
                       (size_t)2 * 16 * D * sizeof(__nv_bfloat16);
@@ -342,7 +365,8 @@ SplitPlan plan_splits(const tv_attn_args *a, int R, bool tc) {
   if (a->num_splits > 0) {
     splits = a->num_splits;
   } else {
-    const long long base = (long long)a->B * a->Hkv * (tc ? 1 : (R + kCcRows - 1) / kCcRows);
+    const int rows_cta = a->D >= 256 ? cc_rows<256>() : cc_rows<128>();
+    const long long base = (long long)a->B * a->Hkv * (tc ? 1 : (R + rows_cta - 1) / rows_cta);
     const long long target = 2LL * sm_count();
     splits = base > 0 ? (int)((target + base - 1) / base) : 1;
   }
