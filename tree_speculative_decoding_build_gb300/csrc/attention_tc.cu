@@ -9,20 +9,29 @@
 // 32 nodes x 4 heads): 128 flop per byte of KV, far beyond what CUDA cores
 // sustain at HBM speed.  R rows are exactly one M = 128 UMMA tile.
 //
-// Design (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: Q tile once per (sequence, KV head) segment, then
-//              64-key K/V tiles (four 16-token paged blocks, 128-byte swizzle)
-//              into a 4-stage shared-memory ring; the tree node K/V rows form
-//              one more tile per segment.
-//   warp 1     TMEM allocation and the single MMA-issuing thread:
-//              S_j = Q K_j^T into a double-buffered TMEM S tile, then
-//              O += P_j V_j (P from TMEM, V read as an MN-major operand).
-//              Every tcgen05.mma of the CTA is issued by this one thread.
-//   warps 2-5  softmax: thread r owns row r; reads S_j from TMEM, applies the
-//              context / window / ancestor mask, keeps the running max and sum,
-//              writes P_j (bf16 pairs) to TMEM, where the P V product reads it.  O is rescaled in
-//              TMEM only when the row max grows by more than 2^8 (the final
-//              division by the running sum makes any reference max exact).
+// Design (one persistent CTA per SM, 11 warps = 352 threads):
+//   warps 0, 10  TMA producers, alternate 64-key tiles: K as eight 2-D boxes
+//                (two 64-dim halves x four 16-token paged blocks, 128-byte
+//                swizzle), V as four 3-D boxes, one copy per lane so the copies
+//                go out together, into a 6-stage 32 KB ring; block ids are read
+//                32 slots at a time one window ahead; the tree node K/V rows
+//                form one more tile per segment.
+//   warp 1       TMEM allocation and the only warp that issues tcgen05.mma (one
+//                elected lane per instruction group; the warp polls its
+//                barriers warp-uniformly and issues a ready P V before a late
+//                S): S_j = Q K_j^T into a double-buffered TMEM S tile (Q read
+//                from TMEM), O_x += P_j V_j (P from TMEM, V read as an MN-major
+//                shared-memory operand).
+//   warps 2-5,   two softmax warpgroups taking alternate tiles, each with its
+//   6-9          own running max / sum and O accumulator in TMEM: thread r owns
+//                row r, reads S_j, frees it at once, applies the context /
+//                window / ancestor mask, writes P_j as bf16 pairs to TMEM.  O is
+//                rescaled in TMEM only when the row max grows by more than 2^8
+//                (the final division by the running sum makes any reference
+//                max exact).  At the end of a (sequence, KV head) segment
+//                warpgroup 0 merges the two O's; it also writes Q into TMEM at
+//                each segment start.
+// TMEM (512 columns): S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448); Q [448,512).
 // Work balance: the (sequence, KV head, tile) list, ragged in sequence length,
 // is cut into equal contiguous ranges, one per CTA.  A (sequence, KV head)
 // pair that falls inside one range is written directly; a pair cut across
