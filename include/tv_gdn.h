@@ -43,10 +43,14 @@ extern "C" {
  *   u       float32 [B, N, Hv, dv]   pseudo-values, kept for tv_gdn_commit
  *   g       float32 [B, N, Hv]       product of alpha along each node's path
  *   kernel  0 auto, 1 CUDA cores (fp32 FMA), 2 tensor cores (tcgen05; d_k 64
- *           or 128).  Auto takes the tensor cores where they apply.  On the
- *           tensor cores K and Q enter as the bf16 they are and the fp32 state
- *           as three bf16 planes (hi + mid + lo, 24 significant bits), with
- *           fp32 accumulation: both kernels give fp32-accurate products.
+ *           or 128; one CTA per sequence, value head and 64 columns of d_v),
+ *           3 tensor cores, persistent pipeline (one CTA per SM over the
+ *           (sequence, value head) problems, the next state in flight while
+ *           the current one is solved; d_k 64 or 128 and N <= 32).  Auto takes
+ *           3, else 2, else 1.  On the tensor cores K and Q enter as the bf16
+ *           they are and the fp32 state as three bf16 planes (hi + mid + lo,
+ *           24 significant bits), with fp32 accumulation: every kernel gives
+ *           fp32-accurate products.
  *   status  int32   [B]              sequences with a non-zero status (a
  *                                    malformed tree) are skipped: their outputs
  *                                    are left untouched; a wait of the
@@ -54,7 +58,7 @@ extern "C" {
  *                                    bound (never on a healthy GPU) writes
  *                                    TV_ERR_CUDA
  * Errors: TV_ERR_ARG (NULL pointers, sizes out of range), TV_ERR_UNSUPPORTED
- * (kernel 2 with d_k not 64 or 128).
+ * (kernel 2 with d_k not 64 or 128; kernel 3 with d_k not 64 or 128 or N > 32).
  */
 tv_status tv_gdn_tree_verify(const float *state, const void *q, const void *k, const void *v,
                              const float *alpha, const float *beta, const uint64_t *anc, int B,

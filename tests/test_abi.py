@@ -131,3 +131,28 @@ def test_graph_host_argument_checks(lib):
     assert lib.tv_verify_graph_launches(None) == 0
     lib.tv_verify_graph_destroy.argtypes = [P]
     lib.tv_verify_graph_destroy(None)
+
+
+def test_gdn_host_argument_checks(lib):
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.tv_gdn_tree_verify.argtypes = [P] * 7 + [I] * 6 + [P] * 3 + [I, P, P]
+    lib.tv_gdn_tree_verify.restype = I
+    nul = [None] * 7
+
+    def verify(B, N, Hk, Hv, dk, dv, kernel):
+        return lib.tv_gdn_tree_verify(*nul, B, N, Hk, Hv, dk, dv, None, None, None, kernel, None,
+                                      None)
+    assert verify(1, 32, 1, 2, 128, 128, 4) == 1    # kernel out of range
+    assert verify(1, 32, 1, 2, 128, 128, -1) == 1
+    assert verify(1, 65, 1, 2, 128, 128, 0) == 1    # N > 64
+    assert verify(1, 32, 2, 3, 128, 128, 0) == 1    # Hv % Hk
+    assert verify(1, 32, 1, 2, 96, 96, 0) == 1      # d_v not a multiple of 64
+    assert verify(1, 32, 1, 2, 96, 128, 2) == 5     # tensor cores: d_k 64 or 128
+    assert verify(1, 33, 1, 2, 128, 128, 3) == 5    # pipeline: N <= 32
+    assert verify(1, 32, 1, 2, 32, 64, 3) == 5      # pipeline: d_k 64 or 128
+    assert verify(0, 32, 1, 2, 128, 128, 3) == 0    # empty batch
+    assert verify(1, 32, 1, 2, 128, 128, 3) == 1    # NULL pointers
+    lib.tv_gdn_commit.argtypes = [P] * 6 + [I] * 6 + [P, P, P]
+    lib.tv_gdn_commit.restype = I
+    assert lib.tv_gdn_commit(*[None] * 6, 1, 32, 1, 2, 128, 128, None, None, None) == 1
+    assert lib.tv_gdn_commit(*[None] * 6, 0, 32, 1, 2, 128, 128, None, None, None) == 0

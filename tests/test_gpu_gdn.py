@@ -66,7 +66,7 @@ def close(got, ref):
     assert err.max() <= 0, f"max excess {err.max():.3e}"
 
 
-CASES = [  # d_k 64 / 128 run on the tensor cores under kernel 0, the rest on CUDA cores
+CASES = [  # kernel 0 picks the pipeline (N <= 32), else the tensor cores (d_k 64 / 128), else CUDA cores
     dict(),                                                       # gdn_small: dk 32, dv 64
     dict(B=2, N=32, Hk=4, Hv=8, dk=128, dv=128),                  # the stress head shape
     dict(B=2, N=64, Hk=1, Hv=2, dk=96, dv=64, tree="chain"),      # depth 64
@@ -75,12 +75,24 @@ CASES = [  # d_k 64 / 128 run on the tensor cores under kernel 0, the rest on CU
     dict(B=3, N=45, Hk=1, Hv=3, dk=128, dv=64),                   # K and Q rows across TMEM quadrants
     dict(B=1, N=1, Hk=1, Hv=1, dk=32, dv=64),                     # a single node
     dict(B=1, N=1, Hk=1, Hv=1, dk=64, dv=64),
+    dict(B=3, N=20, Hk=2, Hv=4, dk=64, dv=64),                    # pipeline: ragged N, d 64 x 64
+    dict(B=2, N=32, Hk=1, Hv=2, dk=128, dv=64, tree="chain"),     # pipeline: depth 32
+    dict(B=5, N=7, Hk=2, Hv=2, dk=128, dv=128, tree="star"),      # pipeline: depth 1, N < 8
+    dict(B=40, N=8, Hk=2, Hv=8, dk=64, dv=64),                    # pipeline: 320 items, > 1 per CTA
 ]
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+def supported(kw, kernel):
+    x = dict(workloads.GDN_WORKLOADS["gdn_small"].__dict__, **kw)
+    tc = x["dk"] in (64, 128)
+    return kernel in (0, 1) or (kernel == 2 and tc) or (kernel == 3 and tc and x["N"] <= 32)
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3])
 @pytest.mark.parametrize("kw", CASES)
 def test_verify_matches_oracle(tv, kw, kernel):
+    if not supported(kw, kernel):
+        pytest.skip("shape outside this kernel")
     x = to_dev(workloads.make_gdn("gdn_small", "cpu", **kw))
     out, u, g, _ = run_verify(tv, x, kernel)
     o = oracle_inputs(x)
@@ -90,7 +102,7 @@ def test_verify_matches_oracle(tv, kw, kernel):
     close(g, ref["g"])
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_verify_full_size_sampled(tv, kernel):
     """The gdn_stress workload (64 sequences x 32 value heads, 128 x 128 state):
     every output computed, four (sequence, head) pairs checked in full."""
@@ -108,13 +120,16 @@ def test_verify_full_size_sampled(tv, kernel):
         close(u[b:b + 1, :, h:h + 1], ref["u"])
 
 
-def test_bad_tree_is_skipped(tv):
-    x = to_dev(workloads.make_gdn("gdn_small", "cpu"))
+@pytest.mark.parametrize("kernel,kw", [(0, dict()), (2, dict(dk=128, dv=128)),
+                                       (3, dict(dk=128, dv=128))])
+def test_bad_tree_is_skipped(tv, kernel, kw):
+    x = to_dev(workloads.make_gdn("gdn_small", "cpu", **kw))
     x["parent"][1, 5] = 7           # parent after the child: tv_build_ancestors flags it
-    out, u, g, st = run_verify(tv, x)
-    assert st.cpu().tolist()[1] != 0
-    assert torch.isnan(out[1]).all() and torch.isnan(u[1]).all()
+    out, u, g, st = run_verify(tv, x, kernel)
+    assert st.cpu().tolist() == [0, st.cpu().tolist()[1], 0] and st.cpu().tolist()[1] != 0
+    assert torch.isnan(out[1]).all() and torch.isnan(u[1]).all() and torch.isnan(g[1]).all()
     assert torch.isfinite(out[0]).all() and torch.isfinite(out[2]).all()
+    assert torch.isfinite(g[0]).all() and torch.isfinite(g[2]).all()
 
 
 @pytest.mark.parametrize("kw", [dict(), dict(B=3, N=32, Hk=4, Hv=8, dk=128, dv=128)])
@@ -140,12 +155,14 @@ def test_commit_matches_oracle(tv, kw):
     assert torch.equal(new[B - 1], x["state"][B - 1])  # empty accept copies S_0 bit for bit
 
 
-def test_tensor_and_cuda_cores_agree(tv):
-    """Both kernels on the same full-size inputs: every output within the
-    tolerance of each other (each is within it of the fp64 oracle)."""
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_tensor_and_cuda_cores_agree(tv, kernel):
+    """A tensor-core kernel and the CUDA-core one on the same full-size inputs:
+    every output within the tolerance of each other (each is within it of the
+    fp64 oracle); g, the same product of the same alphas in the same order, equal."""
     x = to_dev(workloads.make_gdn("gdn_stress", "cpu", B=16))
     o1, u1, g1, _ = run_verify(tv, x, 1)
-    o2, u2, g2, _ = run_verify(tv, x, 2)
+    o2, u2, g2, _ = run_verify(tv, x, kernel)
     close(o2, o1.double().cpu().numpy())
     close(u2, u1.double().cpu().numpy())
     assert torch.equal(g1, g2)

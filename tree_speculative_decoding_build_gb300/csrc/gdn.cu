@@ -23,8 +23,12 @@
 //
 // tv_gdn_commit: one CTA per (sequence, value head, 32 rows of S^T): S_0 read
 // once, the accepted path's rank-n_acc update added, S written once.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -620,6 +624,466 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
   if (w == 0) ptx::tmem_dealloc(tmem, kTcCols);
 }
 
+// ----------------------------------------------------------------------------
+// gdn_tree_verify_pipe_kernel: the same verification as a persistent,
+// warp-specialised pipeline.  One CTA per SM walks the (sequence, value head)
+// items blockIdx.x, blockIdx.x + gridDim.x, ...; while one item is solved the
+// state of the next is in flight.  Trees of at most 32 nodes; d_k 64 or 128,
+// d_v 64 or 128.
+//
+// Roles (12 warps, three warpgroups):
+//   warps 0-3   convert the staged fp32 rows of S_0^T to three bf16 planes in
+//               TMEM (hi + mid + lo = the fp32 value; thread j owns TMEM lane
+//               j = row j); the last warp done with item k sends the TMA of
+//               S_0^T (fp32, [d_v rows][d_k], 128-byte swizzled boxes of 32
+//               columns) for item k + 2 into the staging buffer k leaves, and
+//               warp 2, the only MMA issuer, issues D1 = S_0^T [K; Q]^T (A =
+//               the planes in TMEM, B = the [K; Q] tile) and the node pairs
+//               D2 = [K; Q] K^T;
+//   warps 4-7, 8-11  two post-processing warpgroups, alternate items; each
+//               loads its own items' [K; Q] (32 rows each, bf16, swizzled), V
+//               (32 rows) and, by asynchronous copies, the per-node alpha,
+//               beta, ancestor masks and status word, the next as soon as it
+//               has read the current stage; from
+//               D2 the masked matrices X and Y (one thread per tree row), then
+//               per column j of d_v (thread j, its TMEM lane of D1) the
+//               right-hand sides, the triangular solve for U and the outputs,
+//               dense over the 32 rows (zero off the ancestor pairs) with U in
+//               registers and packed fp32 FMAs.
+// TMEM: two plane buffers (item k in buffer k % 2) at columns 0 and 192, each
+// [0, 3 d_k / 2); one D at 384 (D1, K S_0 then Q S_0, in 64 columns; D2 at
+// 448): the post-processing warps copy it to registers as soon as it is ready,
+// and the MMAs of the next item wait for that (d_empty); d_full[k % 2] tells
+// the warpgroup of item k.  Each wait is bounded
+// (2 s); a wait that runs out raises a CTA-wide abort, every role leaves its
+// loop, copies in flight get a bounded chance to land, and status[b] of the
+// item is set to TV_ERR_CUDA.
+
+constexpr int kPipeN = 32;  // tree rows per tile
+constexpr int kPipeWarps = 12;
+constexpr int kPipeThreads = 32 * kPipeWarps;
+constexpr uint32_t kPipeStage = 25 * 1024;  // [K; Q] halves (2 x 8 KB), V (8 KB), scalars
+constexpr uint32_t kPipeOffV = 16384;
+constexpr uint32_t kPipeOffMeta = 24576;    // alpha [32], beta [32], anc [32], status word
+constexpr uint32_t kPipeOffStg = 2 * kPipeStage;
+constexpr uint32_t kPipeStgBytes = 128 * 128 * 4;  // S_0^T of one head, fp32
+constexpr uint32_t kPipeOffScr = kPipeOffStg + 2 * kPipeStgBytes;
+constexpr int kPipeXS = 36;  // row stride of X and Y (floats; rows 16-byte aligned)
+constexpr uint32_t kPipeScrBytes = (2 * kPipeN * kPipeXS + 2 * kPipeN) * 4;  // X, Y, g, beta
+constexpr uint32_t kPipeSmem = kPipeOffScr + 4 * kPipeScrBytes + 1024;
+constexpr uint32_t kPipeTmemCols = 512;
+constexpr uint32_t kPipeColPlanes = 192;  // planes buffer s at 192 s
+constexpr uint32_t kPipeColD = 384;       // D1 at 384, D2 at 448
+static_assert(kPipeSmem <= 227 * 1024, "shared memory budget");
+
+struct PipeBars {
+  unsigned long long s0_full[2], kqv_full[2];
+  unsigned long long planes_full[2], planes_empty[2];
+  unsigned long long d_full[2], d_empty, wg[2];
+};
+
+__device__ __noinline__ bool pipe_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  const uint64_t t0 = gdn_timer();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (gdn_timer() - t0 > kGdnWaitNs) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+// every lane of the warp waits; true when the phase completed for all of them
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  const bool ok = ptx::mbar_try_wait(bar, parity) || pipe_wait_slow(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 4- or 8-byte asynchronous global -> shared copy; `valid` false writes zeros
+// (source size 0) without reading the source
+__device__ __forceinline__ void cp_async_zfill(uint32_t dst, const void *src, int bytes, bool valid) {
+  const int n = valid ? bytes : 0;
+  if (bytes == 8)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+// x0, x1 -> hi + mid + lo, each a bf16 pair (x0 in the low half); every
+// residual is exact in fp32, so the planes sum to x to 24 bits
+__device__ __forceinline__ void split3(float x0, float x1, uint32_t &h, uint32_t &m, uint32_t &l) {
+  h = ptx::pack_bf16(x0, x1);
+  const float2 r = __fadd2_rn(make_float2(x0, x1),
+                              make_float2(-__uint_as_float(h << 16), -__uint_as_float(h & 0xffff0000u)));
+  m = ptx::pack_bf16(r.x, r.y);
+  const float2 q = __fadd2_rn(r, make_float2(-__uint_as_float(m << 16), -__uint_as_float(m & 0xffff0000u)));
+  l = ptx::pack_bf16(q.x, q.y);
+}
+
+__global__ void __launch_bounds__(kPipeThreads)
+gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_v,
+                            const float *__restrict__ alpha, const float *__restrict__ beta,
+                            const uint64_t *__restrict__ anc, int B, int N, int Hk, int Hv,
+                            int dk, int dv, float *__restrict__ out, float *__restrict__ u_out,
+                            float *__restrict__ g_out, int32_t *__restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ PipeBars bars;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_s0cnt[2];  // warps done with staging buffer s this round
+  __shared__ int s_fills[4];  // copies sent into staging 0, 1 and stage 0, 1
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023) & ~1023u;
+  unsigned char *smem = smem_raw + (sb - raw);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int items = B * Hv;
+  const int nk = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int G = Hv / Hk;
+  const int halves = dk / 64;
+
+  if (w == 2) {
+    ptx::tmem_alloc(ptx::smem_u32(&s_tmem), kPipeTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars.s0_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.kqv_full[i]), 33);
+      s_s0cnt[i] = 0;
+      ptx::mbar_init(ptx::smem_u32(&bars.d_full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.planes_full[i]), 128);
+      ptx::mbar_init(ptx::smem_u32(&bars.planes_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.wg[i]), 128);
+    }
+    ptx::mbar_init(ptx::smem_u32(&bars.d_empty), 128);
+    for (int i = 0; i < 4; ++i) s_fills[i] = 0;
+    s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  volatile int *abort_flag = &s_abort;
+  int fail_b = -1;  // the sequence of the item a role gave up on
+
+  // The copies.  S_0^T of item kk into staging buffer kk % 2 (one thread);
+  // [K; Q], V, the per-node scalars (zero past N) and the status word (zero
+  // without a status array) of item kk into stage kk % 2 (a whole warp; the
+  // scalars by asynchronous copies whose arrival on the stage's barrier fires
+  // once they have landed, so the warp does not wait for them).
+  auto issue_s0 = [&](int kk) {
+    const int item = (int)blockIdx.x + kk * (int)gridDim.x;
+    const uint32_t fb = ptx::smem_u32(&bars.s0_full[kk & 1]);
+    ptx::mbar_arrive_expect_tx(fb, (uint32_t)(dv * dk * 4));
+    const uint32_t dst = sb + kPipeOffStg + (uint32_t)(kk & 1) * kPipeStgBytes;
+    for (int m = 0; m < dk / 32; ++m)
+      ptx::tma_load_2d(dst + (uint32_t)(m * dv * 128), &tm_s, fb, 32 * m, item * dv);
+    s_fills[kk & 1] = kk / 2 + 1;
+  };
+  auto issue_kqv = [&](int kk) {
+    const int item = (int)blockIdx.x + kk * (int)gridDim.x;
+    const int b = item / Hv, h = item - b * Hv, hk = h / G;
+    const int q = kk & 1;
+    const uint32_t st = sb + (uint32_t)q * kPipeStage;
+    const uint32_t fb = ptx::smem_u32(&bars.kqv_full[q]);
+    if (lane == 0) {
+      // rows past N are the next sequence's nodes or zero fill past the end
+      ptx::mbar_arrive_expect_tx(fb, (uint32_t)(halves * 8192 + 64 * dv));
+      for (int hf = 0; hf < halves; ++hf) {
+        ptx::tma_load_2d(st + hf * 8192, &tm_k, fb, hk * dk + 64 * hf, b * N);
+        ptx::tma_load_2d(st + hf * 8192 + 4096, &tm_q, fb, hk * dk + 64 * hf, b * N);
+      }
+      ptx::tma_load_2d(st + kPipeOffV, &tm_v, fb, h * dv, b * N);
+      s_fills[2 + q] = kk / 2 + 1;
+    }
+    const uint32_t meta = st + kPipeOffMeta;
+    const int t = lane;
+    const size_t bt = (size_t)b * N + (t < N ? t : 0);
+    cp_async_zfill(meta + 4 * t, alpha + bt * Hv + h, 4, t < N);
+    cp_async_zfill(meta + 128 + 4 * t, beta + bt * Hv + h, 4, t < N);
+    cp_async_zfill(meta + 256 + 8 * t, anc + bt, 8, t < N);
+    if (t == 0)
+      cp_async_zfill(meta + 512, status ? static_cast<const void *>(status + b) : static_cast<const void *>(alpha), 4,
+                     status != nullptr);
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(fb) : "memory");
+  };
+
+  if (w < 4) {
+    // ---------------------------------------------------------- warpgroup 0
+    // Every warp converts a quarter of the rows (thread j owns TMEM lane j =
+    // row j of S_0^T) into plane buffer k % 2; the last warp done with item k
+    // sends the copy of S_0^T for item k + 2 into the staging buffer item k
+    // leaves; warp 2, the only MMA issuer, then issues the MMAs of item k.
+    const int qd = w, j = 32 * qd + lane;
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+    if (w == 0 && lane == 0) {
+      ptx::prefetch_tensormap(&tm_s);
+      for (int kk = 0; kk < 2 && kk < nk; ++kk) issue_s0(kk);
+    }
+    const uint32_t idesc1 = gdn_idesc(kTcM, 2 * kPipeN);  // D1: N = 64 ([K; Q] rows)
+    const uint32_t idesc2 = gdn_idesc(kTcM, kPipeN);      // D2: N = 32 (K rows)
+    int issued_mma = 0;
+    int k = 0;
+    for (; k < nk; ++k) {
+      const int s = k & 1;
+      // ---- convert item k
+      if (!warp_wait(ptx::smem_u32(&bars.s0_full[s]), (uint32_t)((k >> 1) & 1), abort_flag) ||
+          (k >= 2 && !warp_wait(ptx::smem_u32(&bars.planes_empty[s]), (uint32_t)(((k >> 1) - 1) & 1), abort_flag)))
+        break;
+      ptx::tc_fence_after();
+      const unsigned char *stg = smem + kPipeOffStg + (size_t)s * kPipeStgBytes;
+      for (int m = 0; m < dk / 32; ++m) {
+        float x[32];
+        if (j < dv) {
+          const unsigned char *row = stg + (size_t)m * dv * 128 + (size_t)j * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(row + ((c ^ (j & 7)) << 4));
+            x[4 * c] = v4.x;
+            x[4 * c + 1] = v4.y;
+            x[4 * c + 2] = v4.z;
+            x[4 * c + 3] = v4.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = 0.f;
+        }
+        uint32_t hi[16], mid[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split3(x[2 * e], x[2 * e + 1], hi[e], mid[e], lo[e]);
+        const uint32_t tp = tl + kPipeColPlanes * (uint32_t)s;
+        tmem_st16(tp + (uint32_t)(16 * m), hi);
+        tmem_st16(tp + (uint32_t)(dk / 2 + 16 * m), mid);
+        tmem_st16(tp + (uint32_t)(dk + 16 * m), lo);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.planes_full[s]));
+      // ---- the last of the four warps to leave staging buffer s refills it
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(&s_s0cnt[s], 1) == 3) {
+          s_s0cnt[s] = 0;
+          if (k + 2 < nk) {
+            ptx::fence_proxy_async_smem();
+            issue_s0(k + 2);
+          }
+        }
+      }
+      __syncwarp();
+      // ---- the MMAs of item k (the issuing thread stalls while the tensor
+      //      core's queue is full: about the time the MMAs take)
+      if (w == 2) {
+        const int q = k & 1, n = k >> 1;
+        if (!warp_wait(ptx::smem_u32(&bars.planes_full[q]), (uint32_t)(n & 1), abort_flag) ||
+            !warp_wait(ptx::smem_u32(&bars.kqv_full[q]), (uint32_t)(n & 1), abort_flag) ||
+            (k >= 1 && !warp_wait(ptx::smem_u32(&bars.d_empty), (uint32_t)((k - 1) & 1), abort_flag)))
+          break;
+        ptx::tc_fence_after();
+        const uint32_t kq = sb + (uint32_t)q * kPipeStage;
+        const uint32_t d = tmem + kPipeColD;
+        const uint32_t ap = tmem + kPipeColPlanes * (uint32_t)q;
+        for (int pl = 0; pl < 3; ++pl)
+          for (int kk = 0; kk < dk / 16; ++kk) {
+            const uint64_t bd = gdn_sw128_desc(kq + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u);
+            ptx::umma_f16_ta_warp(d, ap + (uint32_t)(pl * (dk / 2) + kk * 8), bd, idesc1,
+                                  (pl | kk) != 0 ? 1u : 0u);
+          }
+        // A = the [K; Q] tile read as 128 rows (rows past 64 are other data
+        // of the stage: rows of D2 nobody reads), B = its 32 K rows
+        for (int kk = 0; kk < dk / 16; ++kk) {
+          const uint64_t ad = gdn_sw128_desc(kq + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u);
+          ptx::umma_f16_warp(d + 64, ad, ad, idesc2, kk != 0 ? 1u : 0u);
+        }
+        ptx::umma_commit_warp(ptx::smem_u32(&bars.planes_empty[q]));
+        ptx::umma_commit_warp(ptx::smem_u32(&bars.d_full[q]));
+        issued_mma = k + 1;
+      }
+    }
+    if (k < nk) {
+      fail_b = ((int)blockIdx.x + k * (int)gridDim.x) / Hv;
+      if (w == 2 && lane == 0 && issued_mma > 0) {
+        int dummy = 0;  // MMAs in flight finish before TMEM is freed
+        pipe_wait_slow(ptx::smem_u32(&bars.planes_empty[(issued_mma - 1) & 1]),
+                       (uint32_t)(((issued_mma - 1) >> 1) & 1), &dummy);
+      }
+    }
+  } else {
+    // --------------------------------------- X, Y, solve and outputs
+    // warpgroup p takes the items k = p, p + 2, ...: stage and D buffer p
+    const int pb = (w - 4) >> 2, qd = w & 3, j = 32 * qd + lane;
+    // each warpgroup loads its own items' [K; Q], V and scalars: the first
+    // now, the next one as soon as all its warps have read the current stage
+    if (qd == 0 && pb < nk) {
+      if (lane == 0) {
+        ptx::prefetch_tensormap(&tm_k);
+        ptx::prefetch_tensormap(&tm_q);
+        ptx::prefetch_tensormap(&tm_v);
+      }
+      issue_kqv(pb);
+    }
+    for (int k = pb, n = 0; k < nk; k += 2, ++n) {
+      const uint32_t ph = (uint32_t)(n & 1);
+      const int item = (int)blockIdx.x + k * (int)gridDim.x;
+      const int b = item / Hv, h = item - b * Hv;
+      const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16) + kPipeColD;
+      const unsigned char *stage = smem + (size_t)pb * kPipeStage;
+      const float *ma = reinterpret_cast<const float *>(stage + kPipeOffMeta);
+      const float *mb = ma + 32;
+      const uint64_t *mc = reinterpret_cast<const uint64_t *>(stage + kPipeOffMeta + 256);
+      const uint16_t *sv = reinterpret_cast<const uint16_t *>(stage + kPipeOffV);
+      if (!warp_wait(ptx::smem_u32(&bars.kqv_full[pb]), ph, abort_flag) ||
+          !warp_wait(ptx::smem_u32(&bars.d_full[pb]), ph, abort_flag)) {
+        fail_b = b;
+        break;
+      }
+      ptx::tc_fence_after();
+      const bool store = reinterpret_cast<const int *>(stage + kPipeOffMeta + 512)[0] == 0;
+      float *X = reinterpret_cast<float *>(smem + kPipeOffScr + (size_t)(2 * pb + (n & 1)) * kPipeScrBytes);
+      float *Y = X + kPipeN * kPipeXS;
+      float *sg = Y + kPipeN * kPipeXS;
+      float *sbeta = sg + kPipeN;
+      // D2 and both halves of D1 leave TMEM at once, before the next item's
+      // MMAs load the tensor memory, and the D buffer is handed back
+      uint32_t dot[32], ks[32], qs[32];
+      ptx::tmem_ld32(tl + 64, dot);
+      ptx::tmem_ld32(tl, ks);
+      ptx::tmem_ld32(tl + 32, qs);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.d_empty));
+      // 1. node pairs: lanes 0-31 of D2 are K rows, 32-63 Q rows
+      {
+        if (qd < 2) {
+          const int t = lane;
+          const uint64_t msk = mc[t] & ((2ull << t) - 1);  // ancestors-or-self
+          const float bt = mb[t];
+          float *row = (qd == 0 ? X : Y) + t * kPipeXS;
+          float gam = 1.f;  // g_t / g_i, built from alpha going up the path
+#pragma unroll
+          for (int i0 = kPipeN - 4; i0 >= 0; i0 -= 4) {  // four columns at a time
+            const float4 a4 = *reinterpret_cast<const float4 *>(ma + i0);
+            const float al[4] = {a4.x, a4.y, a4.z, a4.w};
+            float rv[4];
+#pragma unroll
+            for (int e = 3; e >= 0; --e) {
+              const int i = i0 + e;
+              const bool a = (msk >> i) & 1;
+              const float dv_i = gam * __uint_as_float(dot[i]);
+              rv[e] = qd == 0 ? ((a && i != t) ? bt * dv_i : 0.f) : (a ? dv_i : 0.f);
+              gam = a ? gam * al[e] : gam;
+            }
+            *reinterpret_cast<float4 *>(row + i0) = make_float4(rv[0], rv[1], rv[2], rv[3]);
+          }
+          if (qd == 0) {
+            sg[t] = gam;
+            sbeta[t] = bt;
+            if (store && t < N) g_out[((size_t)b * N + t) * Hv + h] = gam;
+          }
+        }
+      }
+      // this thread's column of V, then the stage may be refilled
+      uint32_t vcol[kPipeN / 2];
+#pragma unroll
+      for (int e = 0; e < kPipeN / 2; ++e)
+        vcol[e] = j < dv ? (uint32_t)sv[2 * e * dv + j] | ((uint32_t)sv[(2 * e + 1) * dv + j] << 16) : 0u;
+      ptx::mbar_arrive(ptx::smem_u32(&bars.wg[pb]));
+      if (!warp_wait(ptx::smem_u32(&bars.wg[pb]), ph, abort_flag)) {
+        fail_b = b;
+        break;
+      }
+      // the stage is read (V and the scalars by every warp, [K; Q] by the
+      // MMAs behind d_full): the item after next takes it
+      if (qd == 0 && k + 2 < nk) issue_kqv(k + 2);
+      // 2. column j: right-hand sides and forward substitution (K S_0), then
+      //    the outputs (Q S_0)
+      const size_t o0 = ((size_t)b * N * Hv + h) * dv + j, rs = (size_t)Hv * dv;
+      float *uo = u_out + o0, *oo = out + o0;
+      const bool mine = j < dv;
+      // U and the products run on pairs (packed fp32 FMA, one rounding per
+      // element as fmaf): U2[p] = (u_2p, u_2p+1), rows of X and Y in pairs of
+      // columns.  X and Y are zero past each row's own column, and U starts at
+      // zero, so a pair that runs one column past the row adds exact zeros.
+      float2 U2[kPipeN / 2];
+#pragma unroll
+      for (int e = 0; e < kPipeN / 2; ++e) U2[e] = make_float2(0.f, 0.f);
+      if (mine) {
+        // rows in order, each from the rows before it
+#pragma unroll
+        for (int t = 0; t < kPipeN; ++t) {
+          const float vv = __uint_as_float((t & 1) ? (vcol[t >> 1] & 0xffff0000u) : (vcol[t >> 1] << 16));
+          const float r = sbeta[t] * (vv - sg[t] * __uint_as_float(ks[t]));
+          const float *xr = X + t * kPipeXS;
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < t; i += 4) {
+            const float4 c = *reinterpret_cast<const float4 *>(xr + i);
+            acc = __ffma2_rn(make_float2(c.x, c.y), U2[i >> 1], acc);
+            if (i + 2 < t) acc = __ffma2_rn(make_float2(c.z, c.w), U2[(i >> 1) + 1], acc);
+          }
+          const float ut = r - (acc.x + acc.y);
+          if (t & 1) U2[t >> 1].y = ut;
+          else U2[t >> 1].x = ut;
+        }
+        if (store) {
+#pragma unroll
+          for (int t = 0; t < kPipeN; ++t)
+            {
+              if (t < N) *uo = (t & 1) ? U2[t >> 1].y : U2[t >> 1].x;
+              uo += rs;
+            }
+        }
+        // outputs: independent dot products over ancestors-or-self
+#pragma unroll
+        for (int t = 0; t < kPipeN; ++t) {
+          const float *yr = Y + t * kPipeXS;
+          float2 acc = make_float2(sg[t] * __uint_as_float(qs[t]), 0.f);
+#pragma unroll
+          for (int i = 0; i <= t; i += 4) {
+            const float4 c = *reinterpret_cast<const float4 *>(yr + i);
+            acc = __ffma2_rn(make_float2(c.x, c.y), U2[i >> 1], acc);
+            if (i + 2 <= t) acc = __ffma2_rn(make_float2(c.z, c.w), U2[(i >> 1) + 1], acc);
+          }
+          if (store && t < N) *oo = acc.x + acc.y;
+          oo += rs;
+        }
+      }
+    }
+  }
+  if (fail_b >= 0 && lane == 0) set_status(status, fail_b, TV_ERR_CUDA);
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // copies still in flight get a bounded chance to land before exit
+    int dummy = 0;
+    for (int i = 0; i < 4; ++i)
+      if (s_fills[i] > 0)
+        pipe_wait_slow(ptx::smem_u32(i < 2 ? &bars.s0_full[i] : &bars.kqv_full[i - 2]),
+                       (uint32_t)((s_fills[i] - 1) & 1), &dummy);
+  }
+  if (w == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kPipeTmemCols);
+  }
+}
+
 constexpr int kGcThreads = 256;
 
 __host__ __device__ inline size_t gc_k_offset(int N) { return ((size_t)N * 8 + 15) / 16 * 16; }
@@ -698,6 +1162,67 @@ gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__res
   }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 gdn_encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// a 2-D map over rows of `inner` elements, `row_bytes` apart; box0 x box1
+bool gdn_map(CUtensorMap *m, CUtensorMapDataType type, const void *base, uint64_t inner,
+             uint64_t rows, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+             CUtensorMapSwizzle swizzle) {
+  auto fn = gdn_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box0, box1};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// the pipelined kernel's shapes: trees of at most 32 nodes, d_k 64 or 128,
+// coordinates within the 32-bit range of the tensor copies
+bool gdn_pipe_ok(int B, int N, int Hv, int dk, int dv) {
+  return N <= kPipeN && (dk == 64 || dk == 128) && (dv == 64 || dv == 128) &&
+         (uint64_t)B * Hv * dv < (1ull << 31) && (uint64_t)B * N + kPipeN < (1ull << 31);
+}
+
+tv_status launch_gdn_pipe(const float *state, const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                          const __nv_bfloat16 *v, const float *alpha, const float *beta,
+                          const uint64_t *anc, int B, int N, int Hk, int Hv, int dk, int dv,
+                          float *out, float *u, float *g, int32_t *status, cudaStream_t stream) {
+  CUtensorMap ms, mk, mq, mv;
+  const uint64_t rows_s = (uint64_t)B * Hv * dv, rows_n = (uint64_t)B * N;
+  if (!gdn_map(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, state, dk, rows_s, (uint64_t)dk * 4, 32,
+               (uint32_t)dv, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !gdn_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, (uint64_t)Hk * dk, rows_n,
+               (uint64_t)Hk * dk * 2, 64, kPipeN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !gdn_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, (uint64_t)Hk * dk, rows_n,
+               (uint64_t)Hk * dk * 2, 64, kPipeN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !gdn_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, (uint64_t)Hv * dv, rows_n,
+               (uint64_t)Hv * dv * 2, (uint32_t)dv, kPipeN, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return TV_ERR_CUDA;
+  if (cudaFuncSetAttribute(gdn_tree_verify_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kPipeSmem) != cudaSuccess)
+    return TV_ERR_CUDA;
+  const int items = B * Hv;
+  const int grid = items < sm_count() ? items : sm_count();
+  gdn_tree_verify_pipe_kernel<<<grid, kPipeThreads, kPipeSmem, stream>>>(
+      ms, mk, mq, mv, alpha, beta, anc, B, N, Hk, Hv, dk, dv, out, u, g, status);
+  return launch_status();
+}
+
 bool gdn_shape_ok(int B, int N, int Hk, int Hv, int dk, int dv) {
   return B >= 0 && N >= 1 && N <= kGdnMaxN && Hk >= 1 && Hv >= 1 && Hv % Hk == 0 && dk >= 32 &&
          dk <= 128 && dk % 32 == 0 && dv >= 64 && dv <= 128 && dv % 64 == 0;
@@ -714,9 +1239,10 @@ extern "C" tv_status tv_gdn_tree_verify(const float *state, const void *q, const
                                         int dv, float *out, float *u, float *g, int kernel,
                                         int32_t *status, tv_stream stream) {
   if (!gdn_shape_ok(B, N, Hk, Hv, dk, dv)) return TV_ERR_ARG;
-  if (kernel < 0 || kernel > 2) return TV_ERR_ARG;
+  if (kernel < 0 || kernel > 3) return TV_ERR_ARG;
   const bool tc_ok = dk == 64 || dk == 128;
-  if (kernel == 2 && !tc_ok) return TV_ERR_UNSUPPORTED;
+  const bool pipe_ok = gdn_pipe_ok(B, N, Hv, dk, dv);
+  if ((kernel == 2 && !tc_ok) || (kernel == 3 && !pipe_ok)) return TV_ERR_UNSUPPORTED;
   if (B == 0) return TV_OK;
   if (!state || !q || !k || !v || !alpha || !beta || !anc || !out || !u || !g) return TV_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(q) |
@@ -727,6 +1253,11 @@ extern "C" tv_status tv_gdn_tree_verify(const float *state, const void *q, const
   const auto *qb = static_cast<const __nv_bfloat16 *>(q);
   const auto *kb = static_cast<const __nv_bfloat16 *>(k);
   const auto *vb = static_cast<const __nv_bfloat16 *>(v);
+  if (pipe_ok && (kernel == 3 || kernel == 0)) {
+    const tv_status st = launch_gdn_pipe(state, qb, kb, vb, alpha, beta, anc, B, N, Hk, Hv, dk, dv,
+                                         out, u, g, status, as_stream(stream));
+    if (st == TV_OK || kernel == 3) return st;
+  }
   if (tc_ok && kernel != 1) {
     const GdnTcLayout Ly = gdn_tc_layout(N, dk);
     if (cudaFuncSetAttribute(gdn_tree_verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
