@@ -106,9 +106,12 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(workload="stress", batch=None, window_left=None):
     """dram read+write bytes per launch from the committed ncu summary, or None
-    when it is missing or was taken on a different attention source."""
+    when it is missing, was taken on a different attention source, or the run
+    is not the stress workload it describes (64 sequences, global window)."""
+    if workload != "stress" or batch not in (None, 64) or window_left not in (None, -1):
+        return None
     try:
         kv = {}
         with open(TRAFFIC_FILE) as f:
@@ -340,7 +343,8 @@ def bench_ours(args, rank, world, local):
                       "frac_of_peak": achieved / peak, "peak_kind": peak_kind},
         "roofline": {"kernel": "tv_tree_attention", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic(), "peak_source": peak_kind},
+                     "traffic": recorded_traffic(args.workload, args.batch, args.window_left),
+                     "peak_source": peak_kind},
         "e2e": {"value": job_throughput(world, 1, e2e_ms), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
