@@ -599,6 +599,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
     unsigned long long allowed = 0;
     long long seg_f0 = lo;
     bool seg_complete = false;
+    bool q_next_loaded = false;  // Q of the coming segment already in TMEM
     const uint32_t t_p = tlane + kColP + (uint32_t)x * 32;
     while (cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
@@ -610,7 +611,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
         blk_lo = first_visible_block(ctx, wl);
         seg_f0 = cur.f;
         seg_complete = cur.u == 0 && cur.f + (cur.tiles - 1) <= hi - 1;
-        if (x == 0) {
+        if (x == 0 && !q_next_loaded) {
           // Q rows of this (sequence, KV head) into TMEM once the previous
           // segment's last S has read the old ones; rows past R are zero
           if (seg > 0) {
@@ -635,6 +636,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           tc_fence_before();
           mbar_arrive(smem_u32(&bars.q_full));
         }
+        q_next_loaded = false;
         allowed = 0;
         if (row_ok) {
           pos_t = p.pos[(size_t)b * N + t];
@@ -748,6 +750,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           if (!ok) break;
         }
         float2 *mrg = reinterpret_cast<float2 *>(smem + kOffMerge) + (seg & 1) * kM;
+        // is there a next segment in this CTA's range (then warpgroup 1 loads
+        // its Q rows now)
+        const bool q_next = cur.f + 1 < hi && cur.b + (cur.kvh + 1 == p.Hkv ? 1 : 0) < B;
+        q_next_loaded = q_next;
         if (x == 1) {
           // hand (max, sum) to warpgroup 0; wait until it consumed the previous
           // segment's hand-over so the two never drift more than one apart
@@ -759,6 +765,34 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           mrg[m] = make_float2(m_used, l);
           tc_fence_before();
           mbar_arrive(smem_u32(&bars.merge));
+          if (q_next) {
+            // while warpgroup 0 merges, the Q rows of the next segment of this
+            // CTA's range go into TMEM once this segment's last S has read the
+            // old ones (q_empty); that segment's start then skips the load
+            const int nb = cur.kvh + 1 < p.Hkv ? cur.b : cur.b + 1;
+            const int nk = cur.kvh + 1 < p.Hkv ? cur.kvh + 1 : 0;
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + (((size_t)nb * N + t) * p.Hq + nk * G + g) * kD);
+            ok = __all_sync(0xffffffffu,
+                            wait_fast(smem_u32(&bars.q_empty), (uint32_t)(seg & 1), abort_flag));
+            if (!ok) break;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {  // 64 dims at a time
+              uint32_t qn[32];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                const uint4 w = row_ok ? __ldg(src + 8 * hf + v) : make_uint4(0, 0, 0, 0);
+                qn[v * 4 + 0] = w.x;
+                qn[v * 4 + 1] = w.y;
+                qn[v * 4 + 2] = w.z;
+                qn[v * 4 + 3] = w.w;
+              }
+              tmem_st32(tlane + kColQ + 32 * hf, qn);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&bars.q_full));
+          }
         } else {
           ok = __all_sync(0xffffffffu,
                           wait_fast(smem_u32(&bars.merge), (uint32_t)(seg & 1), abort_flag));
