@@ -1089,7 +1089,7 @@ constexpr int kGcThreads = 256;
 __host__ __device__ inline size_t gc_k_offset(int N) { return ((size_t)N * 8 + 15) / 16 * 16; }
 
 // S_out^T[j][i] = g_l S_0^T[j][i] + sum_p gam_p u_p[j] k_p[i] over the accepted path.
-__global__ void __launch_bounds__(kGcThreads)
+__global__ void __launch_bounds__(kGcThreads, 8)
 gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__restrict__ k,
                   const float *__restrict__ u, const float *__restrict__ alpha,
                   const int32_t *__restrict__ acc_nodes, const int32_t *__restrict__ n_acc, int N,
@@ -1104,21 +1104,40 @@ gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__res
   float *sgam = reinterpret_cast<float *>(smem + N * 4);           // [N]
   float *sku = reinterpret_cast<float *>(smem + gc_k_offset(N));   // [N][dk] k rows, 16-aligned
   float *suu = sku + (size_t)N * dk;                               // [N][32] u columns
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {
+    // the accepted path: node indices and their alphas loaded by the lanes
+    // side by side (two per lane, N <= 64), then the products of alpha over
+    // the nodes after each one, in path order from the end (one lane)
+    const int lane = threadIdx.x;
     int L = (status && status[b] != 0) ? 0 : n_acc[b];
     if (L < 0 || L > N) L = 0;
-    for (int p = 0; p < L; ++p) {
-      const int t = acc_nodes[(size_t)b * N + p];
-      if (t < 0 || t >= N) L = 0;
-      spath[p] = t;
+    bool bad = false;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int p = lane + 32 * h2;
+      if (p < L) {
+        const int t = acc_nodes[(size_t)b * N + p];
+        bad |= t < 0 || t >= N;
+        spath[p] = t;
+      }
     }
-    float cur = 1.f;  // product of alpha over the path nodes after p
-    for (int p = L - 1; p >= 0; --p) {
-      sgam[p] = cur;
-      cur *= alpha[((size_t)b * N + spath[p]) * Hv + h];
+    if (__any_sync(0xffffffffu, bad)) L = 0;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int p = lane + 32 * h2;
+      if (p < L) sgam[p] = alpha[((size_t)b * N + spath[p]) * Hv + h];
     }
-    s_len = L;
-    s_gl = cur;  // g of the last node: the product over the whole path
+    __syncwarp();
+    if (lane == 0) {
+      float cur = 1.f;  // product of alpha over the path nodes after p
+      for (int p = L - 1; p >= 0; --p) {
+        const float a = sgam[p];
+        sgam[p] = cur;
+        cur *= a;
+      }
+      s_len = L;
+      s_gl = cur;  // g of the last node: the product over the whole path
+    }
   }
   __syncthreads();
   const int L = s_len;
