@@ -109,18 +109,20 @@ tv_status tv_build_ancestors(const int32_t *parent, const int32_t *depth,
  *   window_right must be -1 or >= 0; every visible key precedes or equals the
  *                query position, so the right bound never removes a key
  *   sm_scale   softmax scale on q.k; 0 means 1/sqrt(D)
- *   num_splits context splits per (sequence, KV head) of the CUDA-core kernel;
- *              0 = chosen by the library (the tensor-core kernel balances its
- *              work itself and ignores it)
+ *   num_splits context splits per (sequence, KV head) of the CUDA-core
+ *              kernel and of the D = 256 tensor-core kernel; 0 = chosen by the
+ *              library (the D = 128 tensor-core kernel balances its work itself
+ *              and ignores it)
  *   kernel     0 = automatic (tensor cores when the shape allows, else CUDA
  *              cores), 1 = CUDA-core kernel, 2 = tensor-core kernel
- *              (TV_ERR_UNSUPPORTED outside its shapes: D = 128,
- *              (Hq/Hkv)*N <= 128, B <= 1024)
- *   max_ctas   at most this many persistent CTAs for the tensor-core kernel,
- *              one per SM (0 = every SM).  Leaving SMs free lets another
- *              kernel that does not depend on this one, such as tv_argmax_sm
- *              on a second stream, run beside it.  Ignored by the CUDA-core
- *              kernel.
+ *              (TV_ERR_UNSUPPORTED outside its shapes: D = 128 with
+ *              (Hq/Hkv)*N <= 128 and B <= 1024, or D = 256 with
+ *              (Hq/Hkv)*N <= 128)
+ *   max_ctas   at most this many persistent CTAs for the D = 128 tensor-core
+ *              kernel, one per SM (0 = every SM).  Leaving SMs free lets
+ *              another kernel that does not depend on this one, such as
+ *              tv_argmax_sm on a second stream, run beside it.  Ignored by the
+ *              other kernels.
  *   out        bf16 [B, N, Hq, D]         softmax(scale q.K^T) V per node and head
  *   status     int32 [B]                  TV_ERR_BLOCK is recorded when a needed
  *                                         block id is outside [0, num_blocks) or

@@ -287,11 +287,17 @@ SMALL = [
     ("best_first", dict(B=2, ctx=(5, 90), N=7, tree="random", V=1000)),       # node tile padded
     ("window", dict(B=5, ctx=(0, 70), N=1, tree="star", window_left=17, V=1000)),
     ("stress", dict(B=40, ctx=(1, 40), V=1000)),   # more (sequence, head) pairs than SMs
+    # head dim 256 (tensor cores since D = 256 has its own kernel)
+    ("leaf_sibling", dict(ctx=1)),
+    ("leaf_sibling", dict(B=3, ctx=(0, 300), V=1000)),                          # ragged, ctx 0
+    ("leaf_sibling", dict(B=2, ctx=(70, 400), N=64, tree="random", V=1000)),    # R = 128 rows
+    ("leaf_sibling", dict(B=2, ctx=(100, 260), N=9, tree="random", window_left=37, V=1000)),
 ]
 
-# (kernel, num_splits): automatic choice (tensor cores for head dim 128), then
-# the CUDA-core kernel with one and with three context splits
-MODES = [(0, 0), (1, 1), (1, 3), (2, 0)]
+# (kernel, num_splits): automatic choice (tensor cores for head dims 128 and
+# 256), then the CUDA-core kernel with one and with three context splits, and
+# the tensor cores asked for explicitly (with three splits at head dim 256)
+MODES = [(0, 0), (1, 1), (1, 3), (2, 0), (2, 3)]
 
 
 @pytest.mark.parametrize("case", range(len(SMALL)))
@@ -300,8 +306,10 @@ def test_attention_small_full_check(tv, case, mode):
     name, kw = SMALL[case]
     kernel, splits = MODES[mode]
     w = workloads.get(name)
-    if kernel == 2 and (w.D != 128 or (w.Hq // w.Hkv) * kw.get("N", w.N) > 128):
-        pytest.skip("the tensor-core kernel covers head dim 128 and <= 128 rows per KV head")
+    if kernel == 2 and (w.D not in (128, 256) or (w.Hq // w.Hkv) * kw.get("N", w.N) > 128):
+        pytest.skip("the tensor-core kernels cover head dims 128 and 256, <= 128 rows per KV head")
+    if kernel == 2 and splits and w.D != 256:
+        pytest.skip("the head-dim-128 tensor-core kernel chooses its own work split")
     inp = workloads.make(name, "cuda", 100 + case, **kw)
     out, st = run_attention(tv, inp, num_splits=splits, kernel=kernel)
     assert (st.cpu().numpy() == 0).all()
@@ -317,9 +325,10 @@ def test_tensor_core_kernel_rejects_other_shapes(tv):
     assert e.value.code == tv.TV_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("name", ["best_first", "leaf_sibling"])
 @pytest.mark.parametrize("kernel", [0, 1])
-def test_attention_bitwise_deterministic_and_block_order_free(tv, kernel):
-    inp = workloads.make("best_first", "cuda", 7, B=4, ctx=(300, 900), V=1000, shuffle_blocks=True)
+def test_attention_bitwise_deterministic_and_block_order_free(tv, kernel, name):
+    inp = workloads.make(name, "cuda", 7, B=4, ctx=(300, 900), V=1000, shuffle_blocks=True)
     a, _ = run_attention(tv, inp, kernel=kernel)
     b, _ = run_attention(tv, inp, kernel=kernel)
     assert torch.equal(a, b)
@@ -335,8 +344,9 @@ def test_attention_bitwise_deterministic_and_block_order_free(tv, kernel):
     assert torch.equal(a, c)
 
 
-def test_attention_bad_block_sets_status(tv):
-    inp = workloads.make("tiny", "cuda", 3, B=2, ctx=(40, 40), N=4, tree="chain", V=64)
+@pytest.mark.parametrize("name", ["tiny", "leaf_sibling"])
+def test_attention_bad_block_sets_status(tv, name):
+    inp = workloads.make(name, "cuda", 3, B=2, ctx=(40, 40), N=4, tree="chain", V=64)
     inp["block_table"] = inp["block_table"].clone()
     inp["block_table"][1, 1] = 10 ** 6
     out, st = run_attention(tv, inp)

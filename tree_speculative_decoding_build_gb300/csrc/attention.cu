@@ -423,6 +423,32 @@ bool use_tc(const tv_attn_args *a) {
   return tc_shape(a);
 }
 
+// The D = 256 tensor-core kernel (split-K, generic partials and combine).
+bool tc256_shape(const tv_attn_args *a) {
+  AttnParams probe{};
+  probe.D = a->D;
+  probe.G = a->Hkv > 0 ? a->Hq / a->Hkv : 0;
+  probe.N = a->N;
+  probe.R = probe.G * a->N;
+  return attention_tc256_supported(probe);
+}
+
+bool use_tc256(const tv_attn_args *a) { return a->kernel != 1 && tc256_shape(a); }
+
+// Splits for the D = 256 tensor-core kernel: about one CTA per SM, each split
+// a whole number of 64-key tiles (four blocks).
+SplitPlan plan_splits_tc256(const tv_attn_args *a) {
+  const int vis = visible_blocks_bound(a->max_blocks, a->window_left);
+  const long long base = (long long)a->B * a->Hkv;
+  int splits = a->num_splits > 0 ? a->num_splits
+                                 : (base > 0 ? (int)((sm_count() + base - 1) / base) : 1);
+  if (splits < 1) splits = 1;
+  int bps = vis > 0 ? (vis + splits - 1) / splits : 4;
+  bps = (bps + 3) / 4 * 4;
+  splits = vis > 0 ? (vis + bps - 1) / bps : 1;
+  return SplitPlan{splits, bps};
+}
+
 size_t workspace_bytes_for(const tv_attn_args *a, int splits) {
   if (splits <= 1) return 0;
   const size_t rows = (size_t)a->B * a->Hkv * splits * (size_t)(a->Hq / a->Hkv) * a->N;
@@ -435,6 +461,7 @@ size_t workspace_bytes_for(const tv_attn_args *a, int splits) {
 extern "C" size_t tv_tree_attention_workspace_size(const tv_attn_args *a) {
   if (!a || !shape_ok(a) || a->Hq % a->Hkv != 0) return 0;
   if (use_tc(a)) return attention_tc_workspace(a->B, sm_count());
+  if (use_tc256(a)) return workspace_bytes_for(a, plan_splits_tc256(a).splits);
   const int R = (a->Hq / a->Hkv) * a->N;
   const SplitPlan sp = plan_splits(a, R, false);
   return workspace_bytes_for(a, sp.splits);
@@ -447,7 +474,7 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   if (a->D != 64 && a->D != 128 && a->D != 256) return TV_ERR_UNSUPPORTED;
   if (a->Hq % a->Hkv != 0) return TV_ERR_ARG;
   if (a->kernel < 0 || a->kernel > 2) return TV_ERR_ARG;
-  if (a->kernel == 2 && !tc_shape(a)) return TV_ERR_UNSUPPORTED;
+  if (a->kernel == 2 && !tc_shape(a) && !tc256_shape(a)) return TV_ERR_UNSUPPORTED;
   const int G = a->Hq / a->Hkv;
   const int R = G * a->N;
   if (R > 256) return TV_ERR_UNSUPPORTED;
@@ -462,7 +489,8 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
                           reinterpret_cast<uintptr_t>(a->v_cache) | reinterpret_cast<uintptr_t>(a->out);
   if (align & 15) return TV_ERR_ARG;
   const bool tc = use_tc(a);
-  const SplitPlan sp = plan_splits(a, R, tc);
+  const bool tc256 = !tc && use_tc256(a);
+  const SplitPlan sp = tc256 ? plan_splits_tc256(a) : plan_splits(a, R, tc);
   const size_t need = tc ? attention_tc_workspace(a->B, sm_count()) : workspace_bytes_for(a, sp.splits);
   if (need > workspace_bytes || (need > 0 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255))))
     return TV_ERR_ARG;
@@ -505,6 +533,11 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   if (tc) {
     if (launch_attention_tc(p, workspace, s) != cudaSuccess) return TV_ERR_CUDA;
     return TV_OK;
+  }
+  if (tc256) {
+    if (launch_attention_tc256(p, s) != cudaSuccess) return TV_ERR_CUDA;
+    if (sp.splits > 1) launch_combine(p, s);
+    return launch_status();
   }
   launch_attention_generic(p, s);
   if (sp.splits > 1) launch_combine(p, s);

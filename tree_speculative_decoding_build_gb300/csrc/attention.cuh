@@ -60,4 +60,9 @@ size_t attention_tc_workspace(int B, int num_ctas);
 // Launches the kernel (one CTA per SM) and its partial combine.
 cudaError_t launch_attention_tc(const AttnParams &p, void *workspace, cudaStream_t stream);
 
+// Tensor-core kernel for D = 256 and R <= 128: one CTA per (sequence, KV
+// head, split) with the split plan's partials (merged by launch_combine).
+bool attention_tc256_supported(const AttnParams &p);
+cudaError_t launch_attention_tc256(const AttnParams &p, cudaStream_t stream);
+
 }  // namespace tv
