@@ -9,18 +9,20 @@
 // Samenvatting: Trees from Marginals (DFlash-TfM)", "2. Boomconstructie" (pop
 // the top w candidates per round).
 //
-// tv_topk: one thread block per row chunk (chunks only when there are too few
-// rows to fill the GPU); each of its warps scans a contiguous eighth of the
-// chunk and keeps a sorted list of its 32 best (value, index) pairs spread over
-// its lanes.  A lane's 16-byte vector is looked at element by element only
-// when its packed maximum beats the list's k-th entry; a ballot hands such
-// vectors to the whole warp, which inserts the winning elements with shuffles.
-// After the first few hundred elements almost no vector passes, so the scan
-// runs at memory speed.  Warp 0 then folds the other warps' lists into its
-// own, and a one-warp-per-row kernel folds the chunk lists of a row.  Order:
-// larger value first, equal values lower index first, NaN as -inf; an empty
-// slot is (-inf, INT32_MAX), which every real element of the row beats, so
-// rows with fewer than k finite values still list real indices.
+// tv_topk: every warp keeps a sorted list of its 32 best (value, index) pairs
+// spread over its lanes.  A lane's 16-byte vector is looked at element by
+// element only when its packed maximum beats the list's k-th entry, so after
+// the first few hundred elements almost no vector is examined and the scan
+// runs at memory speed.  Two plans:
+//  - chunk plan (strided or unaligned rows, small inputs): one thread block
+//    per row chunk, each warp a contiguous eighth of it; a ballot hands a
+//    passing vector to the whole warp, which inserts its winning elements;
+//    warp 0 folds the block's lists and a one-warp-per-row kernel the chunks'.
+//  - stream plan (dense aligned rows): one contiguous range per warp of a
+//    one-CTA-per-SM grid (below).
+// Order: larger value first, equal values lower index first, NaN as -inf; an
+// empty slot is (-inf, INT32_MAX), which every real element of the row beats,
+// so rows with fewer than k finite values still list real indices.
 //
 // tv_build_tree: one warp per sequence.  The candidate heap of the
 // construction holds, for every expanded node, all K of its children; since
@@ -137,6 +139,92 @@ __device__ __forceinline__ void take_flagged(unsigned ballot, const uint4 &q, in
         ti = __shfl_sync(0xffffffffu, li, k - 1);
       }
     }
+  }
+}
+
+// Maximum of a lane's whole load batch (NaN elements ignored): the vectors
+// are folded element-wise first, so the batch costs one horizontal maximum.
+template <typename T, int U>
+__device__ __forceinline__ float batch_max(const uint4 (&q)[U]) {
+  uint4 m = q[0];
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int u = 1; u < U; ++u) {
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m.x) : "r"(q[u].x));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m.y) : "r"(q[u].y));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m.z) : "r"(q[u].z));
+      asm("max.bf16x2 %0, %0, %1;" : "+r"(m.w) : "r"(q[u].w));
+    }
+  } else {
+#pragma unroll
+    for (int u = 1; u < U; ++u) {
+      m.x = __float_as_uint(fmaxf(__uint_as_float(m.x), __uint_as_float(q[u].x)));
+      m.y = __float_as_uint(fmaxf(__uint_as_float(m.y), __uint_as_float(q[u].y)));
+      m.z = __float_as_uint(fmaxf(__uint_as_float(m.z), __uint_as_float(q[u].z)));
+      m.w = __float_as_uint(fmaxf(__uint_as_float(m.w), __uint_as_float(q[u].w)));
+    }
+  }
+  return vec_max<T>(m);
+}
+
+// Lanes with `flag` set hold a vector whose maximum may enter the list.  Each
+// such lane marks, by itself, its elements that beat the k-th entry; the warp
+// then takes the marked elements one at a time (lowest lane first, then lowest
+// element), broadcasting only that pair.  The new k-th entry needs no second
+// shuffle: an insert at position p < k-1 moves the old (k-2)-th entry into
+// place k-1, read in the same step as the insert.  A marked element that no
+// longer beats the k-th entry when its turn comes is dropped, and so is the
+// lane's element `excl` (already in the list).
+template <typename T>
+__device__ __forceinline__ void take_own(bool flag, const uint4 &q, int idx0, int excl, int k,
+                                         float &lv, int &li, float &tv, int &ti) {
+  constexpr int E = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31;
+  unsigned cm = 0;
+  if (flag) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float x = vec_elem<T>(q, e);
+      x = (x != x) ? -INFINITY : x;
+      if (idx0 + e != excl && beats(x, idx0 + e, tv, ti)) cm |= 1u << e;
+    }
+  }
+  unsigned who = __ballot_sync(0xffffffffu, cm != 0);
+  while (who) {
+    const int src = __ffs(who) - 1;
+    // this lane's lowest marked element
+    const int e = __ffs(cm) - 1;
+    float x = -INFINITY;
+#pragma unroll
+    for (int ee = 0; ee < E; ++ee)
+      if (ee == e) x = vec_elem<T>(q, ee);
+    x = (x != x) ? -INFINITY : x;
+    const float bx = __shfl_sync(0xffffffffu, x, src);
+    const int bi = __shfl_sync(0xffffffffu, idx0 + e, src);
+    if (lane == src) cm &= cm - 1;
+    const float t2v = __shfl_sync(0xffffffffu, lv, k >= 2 ? k - 2 : 0);
+    const int t2i = __shfl_sync(0xffffffffu, li, k >= 2 ? k - 2 : 0);
+    if (beats(bx, bi, tv, ti)) {
+      const unsigned m = __ballot_sync(0xffffffffu, beats(bx, bi, lv, li));
+      const int p = __ffs(m) - 1;  // m != 0: lane k-1 at least is beaten
+      const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+      const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+      if (lane > p) {
+        lv = uv;
+        li = ui;
+      } else if (lane == p) {
+        lv = bx;
+        li = bi;
+      }
+      if (p < k - 1) {
+        tv = t2v;
+        ti = t2i;
+      } else {
+        tv = bx;
+        ti = bi;
+      }
+    }
+    who = __ballot_sync(0xffffffffu, cm != 0);
   }
 }
 
@@ -285,9 +373,6 @@ __device__ __forceinline__ unsigned score_key(float f) {
   const unsigned b = __float_as_uint(f);
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
-__device__ __forceinline__ float score_unkey(unsigned k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
 
 // ------------------------------------------------------------------ stream plan
 //
@@ -299,12 +384,54 @@ __device__ __forceinline__ float score_unkey(unsigned k) {
 // the range goes straight to the output, the range's first and last pieces to
 // slots 2w and 2w+1), and a merge kernel folds the pieces of the rows cut by
 // range boundaries.
+//
+// The cost beyond the loads is the inserts, each a chain of warp shuffles
+// (hundreds of cycles while the loads of 15 other warps share the SM), and a
+// warp that inserts much finishes late: its range is fixed.  So:
+//  - a row piece starts with one bitonic fold of the 32 lanes' maxima into the
+//    list (instead of a dozen single inserts), whose k-th entry then bounds
+//    the piece's k-th largest value from below (bar);
+//  - a whole batch inside the row is skipped by one vote on the lanes' batch
+//    maxima when none beats the k-th entry;
+//  - an insert broadcasts only the winning element: the lane that holds it
+//    finds it by itself.
 
 constexpr int kTsWarps = 16;   // warps per CTA
 constexpr int kTsUnroll = 8;   // 16-byte loads per lane per batch (two batches in flight)
 
 __device__ __forceinline__ long long ts_split(long long w, long long nv, long long owners) {
   return w * nv / owners;
+}
+
+// One compare-exchange step of a 32-lane network over (value, index) pairs:
+// this lane ends up with the better pair when keep_better, else the worse.
+__device__ __forceinline__ void cx_step(float &v, int &i, int stride, bool keep_better) {
+  const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+  const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
+  if (keep_better ? beats(ov, oi, v, i) : beats(v, i, ov, oi)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+// Fold 32 candidates, one per lane, into the warp's sorted list (lane 0 the
+// best): bitonic sort of the candidates into ascending order, the better of
+// list[j] and candidate[j] in each lane (the 32 best of both, a bitonic
+// sequence), then a bitonic merge back into descending order.
+__device__ __forceinline__ void fold32(float &lv, int &li, float cv, int ci) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+      // ascending blocks where lane & size == 0 (all of them at size 32)
+      cx_step(cv, ci, stride, ((lane & stride) != 0) == ((lane & size) == 0));
+  if (beats(cv, ci, lv, li)) {
+    lv = cv;
+    li = ci;
+  }
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) cx_step(lv, li, stride, (lane & stride) == 0);
 }
 
 template <typename T>
@@ -325,7 +452,7 @@ topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long lo
   // bar: a lower bound of the current row piece's k-th largest value; values
   // below it cannot be in the piece's k best and are skipped unexamined
   float bar = -INFINITY;
-  bool fresh = true;  // nothing of the current row piece seen yet
+  bool fresh = true;  // no lower bound yet for the current row piece
 
   // close the piece of row r that ends at vector pe
   auto emit = [&](long long pe) {
@@ -359,36 +486,70 @@ topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long lo
 #pragma unroll
     for (int u = 0; u < kTsUnroll; ++u)
       if (b1 + lane + 32 * u < v1) nq[u] = __ldcs(xv + b1 + lane + 32 * u);
-    if (fresh && lim <= rs + vpr - b0) {
-      // the first batch of a row piece lies in one row: its lanes' maxima are
-      // 32 distinct values of the piece, so the k-th largest of them bounds the
-      // piece's k-th largest from below
-      float lm = -INFINITY;
-#pragma unroll
-      for (int u = 0; u < kTsUnroll; ++u)
-        if (lane + 32 * u < lim) lm = fmaxf(lm, vec_max<T>(q[u]));
-      unsigned key = lm == lm ? score_key(lm) : 0u;
-      unsigned kth = 0;
-      for (int j = 0; j < k; ++j) {
-        kth = __reduce_max_sync(0xffffffffu, key);
-        const unsigned hit = __ballot_sync(0xffffffffu, key == kth);
-        if (lane == __ffs(hit) - 1) key = 0;  // each lane maximum counts once
+    // The common case: a whole batch inside the current row with k entries in
+    // the list.  A batch whose lanes' maxima do not beat the k-th entry (or
+    // lie below bar) holds nothing for the list: one vote skips it.
+    if (!fresh && ti != INT32_MAX && lim == kBatch && b1 <= rs + vpr) {
+      const float bm = batch_max<T>(q);
+      if (!__any_sync(0xffffffffu, bm > tv && !(bm < bar))) {
+        if (b1 == rs + vpr) {
+          emit(b1);
+          ++r;
+          rs += vpr;
+        }
+        continue;
       }
-      if (kth != 0) bar = score_unkey(kth);
     }
-    fresh = false;
     int ps = 0;  // piece [ps, pe) of this batch lies in row r (offsets from b0)
     while (ps < lim) {
       const int pe = (int)min((long long)lim, rs + vpr - b0);
       const int base = (int)((b0 - rs) * E);  // row-local index of vector b0
+      int excl = -1;  // a lane's element already in the list, not to be taken twice
+      // After a fold the list holds elements from all over this batch, so a
+      // vector here whose maximum ties the k-th entry may still hold a lower
+      // index that beats it; elsewhere every list entry precedes the batch.
+      bool folded = false;
+      if (fresh) {
+        // No bound yet for this row piece (it starts here, at a range start or
+        // in the middle of the batch after a row end).  Each lane's best
+        // element in [ps, pe) goes into the list in one fold (32 candidates at
+        // once instead of one insert each); with k of them in, the k-th entry
+        // bounds the piece's k-th largest from below.
+        float lm = -INFINITY;
+        int im = INT32_MAX;
+#pragma unroll
+        for (int u = 0; u < kTsUnroll; ++u) {
+          const int j = lane + 32 * u;
+          if (j >= ps && j < pe) {
+            const float m = vec_max<T>(q[u]);
+            if (m > lm) {  // the earliest vector holding the lane's maximum
+              int e = E - 1;
+#pragma unroll
+              for (int ee = E - 1; ee >= 0; --ee)
+                if (vec_elem<T>(q[u], ee) == m) e = ee;
+              lm = m;
+              im = base + j * E + e;
+            }
+          }
+        }
+        fold32(lv, li, lm, im);
+        tv = __shfl_sync(0xffffffffu, lv, k - 1);
+        ti = __shfl_sync(0xffffffffu, li, k - 1);
+        excl = im;
+        folded = true;
+        if (ti != INT32_MAX) {
+          bar = tv;
+          fresh = false;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < kTsUnroll; ++u) {
         const int j = lane + 32 * u;
         const bool in = j >= ps && j < pe;
         const float m = vec_max<T>(q[u]);
-        const bool flag = in && (m > tv || ti == INT32_MAX) && !(m < bar);
+        const bool flag = in && (m > tv || (folded && m == tv) || ti == INT32_MAX) && !(m < bar);
         const unsigned ballot = __ballot_sync(0xffffffffu, flag);
-        if (ballot) take_flagged<T>(ballot, q[u], base + j * E, k, lv, li, tv, ti);
+        if (ballot) take_own<T>(flag, q[u], base + j * E, excl, k, lv, li, tv, ti);
       }
       if (b0 + pe == rs + vpr) {
         emit(b0 + pe);
