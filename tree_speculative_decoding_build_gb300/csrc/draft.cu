@@ -399,8 +399,22 @@ __device__ __forceinline__ unsigned score_key(float f) {
 constexpr int kTsWarps = 16;   // warps per CTA
 constexpr int kTsUnroll = 8;   // 16-byte loads per lane per batch (two batches in flight)
 
-__device__ __forceinline__ long long ts_split(long long w, long long nv, long long owners) {
-  return w * nv / owners;
+// The split weighs row starts: each row counts as `pen` empty slots followed
+// by its vpr vectors, and the virtual total tot = rows * (vpr + pen) is cut
+// evenly, so a warp whose range holds a row start (a second row piece, with
+// its own list to build) is given pen fewer vectors.  First vector of warp w:
+__device__ __forceinline__ long long ts_split(long long w, long long vpr, long long pen,
+                                              long long tot, long long owners) {
+  const long long y = w * tot / owners;
+  const long long row = y / (vpr + pen), off = y - row * (vpr + pen);
+  return row * vpr + (off > pen ? off - pen : 0);
+}
+// The warp whose range holds vector x: the last w with split(w) <= x.
+__device__ __forceinline__ long long ts_owner(long long x, long long vpr, long long pen,
+                                              long long tot, long long owners) {
+  const long long row = x / vpr;
+  const long long y = row * (vpr + pen) + pen + (x - row * vpr);
+  return ((y + 1) * owners + tot - 1) / tot - 1;  // ceil((y + 1) * owners / tot) - 1
 }
 
 // One compare-exchange step of a 32-lane network over (value, index) pairs:
@@ -436,7 +450,8 @@ __device__ __forceinline__ void fold32(float &lv, int &li, float cv, int ci) {
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kTsWarps, 1)
-topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long long owners, int k,
+topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long long pen,
+                   long long tot, long long owners, int k,
                    float *__restrict__ part_v, int32_t *__restrict__ part_i,
                    float *__restrict__ out_v, int32_t *__restrict__ out_i) {
   constexpr int E = 16 / sizeof(T);
@@ -444,7 +459,8 @@ topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long lo
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kTsWarps + (threadIdx.x >> 5);
   if (w >= owners) return;
-  const long long v0 = ts_split(w, nv, owners), v1 = ts_split(w + 1, nv, owners);
+  const long long v0 = ts_split(w, vpr, pen, tot, owners);
+  const long long v1 = ts_split(w + 1, vpr, pen, tot, owners);
   const uint4 *xv = reinterpret_cast<const uint4 *>(x);
   long long r = v0 / vpr, rs = r * vpr;
   float lv = -INFINITY, tv = -INFINITY;
@@ -565,21 +581,20 @@ topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long lo
 // Rows cut by range boundaries: warp p-1 of the grid owns boundary p when p is
 // the first boundary inside its row, and folds that row's pieces.
 __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
-                                         const int32_t *__restrict__ part_i, long long nv,
-                                         long long vpr, long long owners, int k,
+                                         const int32_t *__restrict__ part_i, long long vpr,
+                                         long long pen, long long tot, long long owners, int k,
                                          float *__restrict__ out_v, int32_t *__restrict__ out_i) {
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5) + 1;
   const int lane = threadIdx.x & 31;
   if (p >= owners) return;
-  const long long bnd = ts_split(p, nv, owners);
+  const long long bnd = ts_split(p, vpr, pen, tot, owners);
   const long long r = bnd / vpr, rs = r * vpr;
   if (bnd == rs) return;                          // on a row start: nothing cut
-  if (ts_split(p - 1, nv, owners) > rs) return;   // an earlier boundary owns this row
+  if (ts_split(p - 1, vpr, pen, tot, owners) > rs) return;  // an earlier boundary owns this row
   const long long c0 = p - 1;
-  const long long xl = rs + vpr - 1;              // owner of the row's last vector:
-  const long long c1 = ((xl + 1) * owners + nv - 1) / nv - 1;  // ceil((x+1)*owners/nv) - 1
-  // the pieces' lists, 32 candidates per step, one per lane; only candidates
-  // that beat the current k-th entry are inserted (a ballot hands them over)
+  const long long c1 = ts_owner(rs + vpr - 1, vpr, pen, tot, owners);  // owner of the row's end
+  // the pieces' lists, 32 candidates per step, one per lane, folded into the
+  // list at once (steps where none beats the k-th entry are skipped)
   float lv = -INFINITY, tv = -INFINITY;
   int li = INT32_MAX, ti = INT32_MAX;
   const long long total = (c1 - c0 + 1) * k;
@@ -590,25 +605,17 @@ __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
     if (qq < total) {
       const long long c = c0 + qq / k;
       const int jj = (int)(qq - (qq / k) * k);
-      const long long s0 = ts_split(c, nv, owners);
-      if (s0 != ts_split(c + 1, nv, owners)) {  // empty ranges wrote nothing
+      const long long s0 = ts_split(c, vpr, pen, tot, owners);
+      if (s0 != ts_split(c + 1, vpr, pen, tot, owners)) {  // empty ranges wrote nothing
         const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
         x = part_v[slot * k + jj];
         xi = part_i[slot * k + jj];
       }
     }
-    unsigned ballot = __ballot_sync(0xffffffffu, xi != INT32_MAX && beats(x, xi, tv, ti));
-    while (ballot) {
-      const int src = __ffs(ballot) - 1;
-      ballot &= ballot - 1;
-      const float y = __shfl_sync(0xffffffffu, x, src);
-      const int yi = __shfl_sync(0xffffffffu, xi, src);
-      if (beats(y, yi, tv, ti)) {
-        wl_insert(lv, li, y, yi);
-        tv = __shfl_sync(0xffffffffu, lv, k - 1);
-        ti = __shfl_sync(0xffffffffu, li, k - 1);
-      }
-    }
+    if (!__any_sync(0xffffffffu, xi != INT32_MAX && beats(x, xi, tv, ti))) continue;
+    fold32(lv, li, x, xi);
+    tv = __shfl_sync(0xffffffffu, lv, k - 1);
+    ti = __shfl_sync(0xffffffffu, li, k - 1);
   }
   if (lane < k) {
     out_v[r * k + lane] = lv;
@@ -625,6 +632,12 @@ struct TopkPlan {
   int ctas;        // stream plan
   size_t pairs;    // partial (value, index) pairs the plan writes
 };
+
+// Row-start weight of the stream plan's range split, in 16-byte vectors.
+// Measured on 512 and 1024 rows of 151936 fp32: 2048 to 6144 vectors (one to
+// three row pieces' worth of list building) take 6 to 8 % off the scan; small
+// rows get an eighth of a row.
+long long topk_row_penalty(long long vpr) { return vpr / 8 < 3072 ? vpr / 8 : 3072; }
 
 bool topk_stream_shape(long long rows, long long V, int esize) {
   return (V * esize) % 16 == 0 && rows * V * esize >= 32768LL * sm_count();
@@ -863,15 +876,18 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
     const long long vpr = V * esize / 16;
     const long long nv = rows * vpr;
     const long long owners = (long long)p.ctas * kTsWarps;
+    const long long pen = topk_row_penalty(vpr);
+    const long long tot = rows * (vpr + pen);
     if (dtype == TV_BF16)
       topk_stream_kernel<__nv_bfloat16><<<p.ctas, 32 * kTsWarps, 0, s>>>(
-          static_cast<const __nv_bfloat16 *>(x), nv, vpr, owners, k, pv, pi, out_vals, out_idx);
+          static_cast<const __nv_bfloat16 *>(x), nv, vpr, pen, tot, owners, k, pv, pi, out_vals,
+          out_idx);
     else
       topk_stream_kernel<float><<<p.ctas, 32 * kTsWarps, 0, s>>>(
-          static_cast<const float *>(x), nv, vpr, owners, k, pv, pi, out_vals, out_idx);
+          static_cast<const float *>(x), nv, vpr, pen, tot, owners, k, pv, pi, out_vals, out_idx);
     const int wpb = 8;
     topk_stream_merge_kernel<<<(unsigned)((owners - 1 + wpb - 1) / wpb), 32 * wpb, 0, s>>>(
-        pv, pi, nv, vpr, owners, k, out_vals, out_idx);
+        pv, pi, vpr, pen, tot, owners, k, out_vals, out_idx);
     return launch_status();
   }
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((row_stride * esize) % 16 == 0);
