@@ -542,7 +542,10 @@ def bench_draft(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "impl": "ours", "path": "draft",
         "config": {"workload": r["workload"], "batch": B,
-                   "l2": "inputs larger than L2 (311 MB of log-probs per step)"},
+                   "l2": (f"inputs larger than L2 ({r['tv_topk']['bytes'] / 1e6:.0f} MB of "
+                          "log-probs per step)" if r["tv_topk"]["bytes"] > 129e6 else
+                          f"inputs L2-resident ({r['tv_topk']['bytes'] / 1e6:.0f} MB of "
+                          "log-probs per step, reused)")},
         "roofline": {"kernel": "tv_topk", "bound": "hbm", "achieved": r["tv_topk"]["gbs"],
                      "peak": r["tv_topk"]["peak"], "unit": "GB/s",
                      "frac": r["tv_topk"]["frac_of_peak"], "traffic": None,
