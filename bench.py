@@ -667,9 +667,22 @@ def measure_gdn(name, steps, warmup, dev, batch=None, seed_offset=0):
     u = torch.empty_like(out)
     g = torch.empty(B, N, Hv, device=dev)
     new = torch.empty_like(x["state"])
-    # accepted path per sequence: node 0's ancestors-or-self (a root) extended to its deepest child chain
-    acc = torch.zeros(B, N, dtype=torch.int32, device=dev)
-    n_acc = torch.ones(B, dtype=torch.int32, device=dev)
+    # accepted path per sequence: root to the first node at depth min(4, deepest), a
+    # typical accepted length (the path's nodes are its ancestors-or-self, root first)
+    par, dep = x["parent"].cpu(), x["depth"].cpu()
+    acc_h = torch.zeros(B, N, dtype=torch.int32)
+    n_acc_h = torch.zeros(B, dtype=torch.int32)
+    for b in range(B):
+        want = min(4, int(dep[b].max()))
+        t = int((dep[b] == want).nonzero()[0, 0])
+        path = []
+        while t >= 0:
+            path.append(t)
+            t = int(par[b, t])
+        path.reverse()
+        acc_h[b, :len(path)] = torch.tensor(path, dtype=torch.int32)
+        n_acc_h[b] = len(path)
+    acc, n_acc = acc_h.to(dev), n_acc_h.to(dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
