@@ -774,6 +774,10 @@ build_tree_kernel(const float *cand_lp, const int32_t *cand_idx, int B, int L, i
   while (n < budget) {
     const int start = n;
     const int take = min(w, budget - n);
+    // children cursors opened by this round's nodes, set up in the registers
+    // of the lanes that own them and opened when the round ends
+    unsigned pend = 0;  // bit u: this lane's cursor u opens at the round's end
+    int pushes = 0;  // this round's popped nodes with children, so far
     for (int q = 0; q < take; ++q) {
       // this lane's best cursor: higher score, then lower counter
       unsigned bk = 0;
@@ -787,12 +791,20 @@ build_tree_kernel(const float *cand_lp, const int32_t *cand_idx, int B, int L, i
         }
       const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
       if (wk == 0) break;  // the heap ran empty: the round ends early
-      const unsigned wc = __reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bc : 0xffffffffu);
-      const unsigned win = __ballot_sync(0xffffffffu, bk == wk && (unsigned)bc == wc);
-      if (lane == __ffs(win) - 1) {
+      unsigned win = __ballot_sync(0xffffffffu, bk == wk);
+      if (win & (win - 1)) {  // tied scores: the lower push counter wins
+        const unsigned wc = __reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bc : 0xffffffffu);
+        win = __ballot_sync(0xffffffffu, bk == wk && (unsigned)bc == wc);
+      }
+      const int src = __ffs(win) - 1;
+      float psc = 0.f;
+      int pdep = 0;
+      if (lane == src) {
 #pragma unroll
         for (int u = 0; u < kBtSlots; ++u) {  // static indices keep the cursors in registers
           if (u == bu) {
+            psc = sc[u];
+            pdep = dep[u];
             s.node_score[n] = sc[u];
             s.node_tok[n] = tk[(size_t)(dep[u] - 1) * K + nr[u]];
             s.node_par[n] = lane + 32 * u - 1;
@@ -802,26 +814,33 @@ build_tree_kernel(const float *cand_lp, const int32_t *cand_idx, int B, int L, i
           }
         }
       }
+      // node n's children are cursor n+1 (lane (n+1) % 32, slot (n+1) / 32),
+      // with the next K push counters in pop order
+      psc = __shfl_sync(0xffffffffu, psc, src);
+      pdep = __shfl_sync(0xffffffffu, pdep, src);
+      if (pdep < L) {
+        const bool mine = lane == ((n + 1) & 31);
+        const int tu = (n + 1) >> 5;
+#pragma unroll
+        for (int u = 0; u < kBtSlots; ++u) {  // selects, not a store at a computed index
+          const bool m = mine && tu == u;
+          pend |= m ? 1u << u : 0u;
+          cb[u] = m ? counter + K * pushes : cb[u];
+          dep[u] = m ? pdep + 1 : dep[u];
+          base[u] = m ? psc : base[u];
+        }
+        ++pushes;
+      }
       ++n;
     }
     if (n == start) break;  // nothing left to pop: the K-ary tree of depth L is complete
-    __syncwarp();
-    // after the round, its nodes push their children, in pop order: node t
-    // (depth < L) opens cursor t+1 with the next K push counters
 #pragma unroll
-    for (int u = 0; u < kBtSlots; ++u) {
-      const int t = lane + 32 * u - 1;
-      if (t >= start && t < n && s.node_dep[t] < L) {
-        int before = 0;
-        for (int t2 = start; t2 < t; ++t2) before += s.node_dep[t2] < L;
+    for (int u = 0; u < kBtSlots; ++u)
+      if (pend & (1u << u)) {
         nr[u] = 0;
-        cb[u] = counter + K * before;
-        dep[u] = s.node_dep[t] + 1;
-        base[u] = s.node_score[t];
         bt_refresh(lp, K, nr[u], cb[u], dep[u], base[u], key[u], cnt[u], sc[u]);
       }
-    }
-    for (int t = start; t < n; ++t) counter += s.node_dep[t] < L ? K : 0;
+    counter += K * pushes;
   }
   __syncwarp();
   for (int t = lane; t < budget; t += 32) {
