@@ -71,6 +71,66 @@ def rank_seed(name, rank):
     return workloads.get(name).seed + rank
 
 
+def pipelined_e2e(step, host, bufs, results, E, stream, dev, copy_streams=4):
+    """Milliseconds per step, end to end: every step uploads its inputs from pinned
+    host memory, runs, and reads its results back, inside the timed region.  The
+    device inputs are double-buffered, so step s+1's upload (on copy streams, big
+    tensors cut into one chunk per stream to use several copy engines) overlaps
+    step s; an upload waits until the step that last used its buffer is done."""
+    import torch
+    css = [torch.cuda.Stream(device=dev) for _ in range(copy_streams)]
+    up = [[torch.cuda.Event() for _ in css] for _ in bufs]
+    used = [torch.cuda.Event() for _ in bufs]
+
+    def upload(b, after):
+        for cs in css:
+            cs.wait_event(after)
+        j = 0
+        for k, src in host.items():
+            dst = bufs[b][k]
+            nbytes = src.numel() * src.element_size()
+            if nbytes >= (64 << 20):
+                flat_s, flat_d = src.view(-1), dst.view(-1)
+                n = flat_s.numel()
+                for c, cs in enumerate(css):
+                    lo, hi = n * c // len(css), n * (c + 1) // len(css)
+                    with torch.cuda.stream(cs):
+                        flat_d[lo:hi].copy_(flat_s[lo:hi], non_blocking=True)
+            else:
+                with torch.cuda.stream(css[j % len(css)]):
+                    dst.copy_(src, non_blocking=True)
+                j += 1
+        for cs, ev in zip(css, up[b]):
+            ev.record(cs)
+
+    def compute(b):
+        for ev in up[b]:
+            stream.wait_event(ev)
+        step(bufs[b])
+        for dst, src in results:
+            dst.copy_(src, non_blocking=True)
+        used[b].record(stream)
+
+    def run(steps, e_start):
+        upload(0, e_start)
+        for s in range(steps):
+            nb = (s + 1) % len(bufs)
+            if s + 1 < steps:
+                upload(nb, used[nb] if s + 1 >= len(bufs) else e_start)
+            compute(s % len(bufs))
+
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(2, e0)  # warm-up
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    run(E, e0)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / E
+
+
 def max_over_ranks(x, world, device):
     """The largest of every rank's ``x`` (a time), on every rank."""
     if world == 1:
@@ -295,27 +355,10 @@ def bench_ours(args, rank, world, local):
     res_keys = ["out_tokens", "n_emit", "n_acc", "ctx_len_out"]
     res_host = {k: torch.empty_like(getattr(o, k), device="cpu").pin_memory() for k in res_keys}
     d2h = sum(v.numel() * v.element_size() for v in res_host.values())
-    dev_inp = dict(inp)
-    for _ in range(2):
-        for k in host_keys:
-            dev_inp[k].copy_(host[k], non_blocking=True)
-        step(dev_inp)
-        for k in res_keys:
-            res_host[k].copy_(getattr(o, k), non_blocking=True)
-    torch.cuda.synchronize(dev)
-    E = max(1, args.e2e_steps)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        for k in host_keys:
-            dev_inp[k].copy_(host[k], non_blocking=True)
-        step(dev_inp)
-        for k in res_keys:
-            res_host[k].copy_(getattr(o, k), non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / E
+    bufs = [dict(inp)] + [dict(inp, **{k: torch.empty_like(inp[k]) for k in host_keys})]
+    results = [(res_host[k], getattr(o, k)) for k in res_keys]
+    e2e_ms = pipelined_e2e(lambda d: step(d), host, bufs, results, max(1, args.e2e_steps),
+                           stream, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     if rank != 0:
@@ -519,21 +562,13 @@ def bench_draft(args, rank, world, local):
     w = workloads.DRAFT_WORKLOADS[args.draft_workload]
     B = lp.shape[0]
     dt = tv.DraftTree(B, w.L, w.V, w.K, w.budget, w.w, device=dev)
-    E = max(1, args.e2e_steps)
     stream = torch.cuda.current_stream(dev)
-    for it in range(E + 2):
-        if it == 2:
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        lp.copy_(lp_host, non_blocking=True)
-        oo = dt(lp)
-        for h, t in zip(res_host, [oo.tokens, oo.parent, oo.depth, oo.n_nodes]):
-            h.copy_(t, non_blocking=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / E, world, dev)
+    oo = dt(lp)  # the outputs live in fixed buffers
+    results = list(zip(res_host, [oo.tokens, oo.parent, oo.depth, oo.n_nodes]))
+    bufs = [{"lp": lp}, {"lp": torch.empty_like(lp)}]
+    e2e_ms = pipelined_e2e(lambda d: dt(d["lp"]), {"lp": lp_host}, bufs, results,
+                           max(1, args.e2e_steps), stream, dev)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     if rank != 0:
         return None
     line = {
