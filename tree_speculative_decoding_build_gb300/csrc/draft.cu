@@ -450,8 +450,8 @@ __device__ __forceinline__ void fold32(float &lv, int &li, float cv, int ci) {
 
 template <typename T>
 __global__ void __launch_bounds__(32 * kTsWarps, 1)
-topk_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long long pen,
-                   long long tot, long long owners, int k,
+topk_stream_kernel(const T *__restrict__ x, long long vpr, long long pen, long long tot,
+                   long long owners, int k,
                    float *__restrict__ part_v, int32_t *__restrict__ part_i,
                    float *__restrict__ out_v, int32_t *__restrict__ out_i) {
   constexpr int E = 16 / sizeof(T);
@@ -893,17 +893,16 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
   cudaStream_t s = as_stream(stream);
   if (p.stream) {
     const long long vpr = V * esize / 16;
-    const long long nv = rows * vpr;
     const long long owners = (long long)p.ctas * kTsWarps;
     const long long pen = topk_row_penalty(vpr);
     const long long tot = rows * (vpr + pen);
     if (dtype == TV_BF16)
       topk_stream_kernel<__nv_bfloat16><<<p.ctas, 32 * kTsWarps, 0, s>>>(
-          static_cast<const __nv_bfloat16 *>(x), nv, vpr, pen, tot, owners, k, pv, pi, out_vals,
+          static_cast<const __nv_bfloat16 *>(x), vpr, pen, tot, owners, k, pv, pi, out_vals,
           out_idx);
     else
       topk_stream_kernel<float><<<p.ctas, 32 * kTsWarps, 0, s>>>(
-          static_cast<const float *>(x), nv, vpr, pen, tot, owners, k, pv, pi, out_vals, out_idx);
+          static_cast<const float *>(x), vpr, pen, tot, owners, k, pv, pi, out_vals, out_idx);
     const int wpb = 8;
     topk_stream_merge_kernel<<<(unsigned)((owners - 1 + wpb - 1) / wpb), 32 * wpb, 0, s>>>(
         pv, pi, vpr, pen, tot, owners, k, out_vals, out_idx);

@@ -58,7 +58,6 @@ __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src)
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
-constexpr int kGdnRows = kGdnMaxN / kGdnWarps;  // rows per warp at most
 
 struct GdnLayout {
   int N, dk;
