@@ -149,15 +149,37 @@ def test_build_tree_matches_oracle(tv, L, K, budget, w):
     assert_tree_equal(got, exp)
 
 
+@pytest.mark.parametrize("budget", [32, 64])
 @pytest.mark.parametrize("w", [1, 2, 5])
-def test_build_tree_ties_follow_push_order(tv, w):
+def test_build_tree_ties_follow_push_order(tv, w, budget):
     """Logits on a 0.5 grid: many exactly tied log-probabilities and scores."""
     B, L, K = 32, 6, 12
     vals, idx = candidates(B, L, 200, K, seed=77 + w, quantum=0.5)
     assert any(len(set(r.tolist())) < K for r in vals.reshape(-1, K))  # ties exist
-    got = run_tree(tv, vals, idx, 64, w)
-    exp = tb.build_tree(vals, idx, 64, w)
+    got = run_tree(tv, vals, idx, budget, w)
+    exp = tb.build_tree(vals, idx, budget, w)
     assert_tree_equal(got, exp)
+
+
+@pytest.mark.parametrize("budget", [32, 64])
+@pytest.mark.parametrize("w", [1, 3])
+def test_build_tree_ties_and_signed_zeros(tv, budget, w):
+    """Candidate values on a 0.5 grid around zero, zeros stored as -0 or +0 at
+    random: many exact ties, scores that sum to +0 or -0.  The two zeros
+    compare equal, so the push counter decides between them; the scores keep
+    their sign bits."""
+    rng = np.random.default_rng(400 + budget + w)
+    B, L, K = 40, 5, 6
+    vals = (rng.integers(-4, 5, (B, L, K)) * 0.5).astype(np.float32)
+    vals = -np.sort(-vals, axis=-1)
+    neg = rng.random((B, L, K)) < 0.5
+    vals = np.where((vals == 0) & neg, np.float32(-0.0), vals).astype(np.float32)
+    assert (np.signbit(vals) & (vals == 0)).any() and (~np.signbit(vals) & (vals == 0)).any()
+    idx = np.arange(B * L * K, dtype=np.int32).reshape(B, L, K)
+    got = run_tree(tv, vals, idx, budget, w)
+    exp = tb.build_tree(vals, idx, budget, w)
+    assert_tree_equal(got, exp)
+    assert np.array_equal(got["score"].view(np.int32), exp["score"].view(np.int32))
 
 
 def test_build_tree_minus_inf_candidates(tv):

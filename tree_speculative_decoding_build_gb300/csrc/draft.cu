@@ -369,8 +369,11 @@ __global__ void topk_merge_kernel(const float *__restrict__ part_v, const int32_
 }
 
 // Order-preserving unsigned key of a non-NaN float; 0 is below every float.
+// -0 keys as +0: the two compare equal, so a tie between them goes to the
+// push counter.
 __device__ __forceinline__ unsigned score_key(float f) {
-  const unsigned b = __float_as_uint(f);
+  unsigned b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
