@@ -69,7 +69,8 @@ tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, int64_t row
  * the float32 sum of the log-probabilities along its path, added in depth order.
  * The candidate heap starts with the K depth-1 candidates (the roots); each
  * round pops the min(w, budget - n) best candidates (higher score first, equal
- * scores in push order) and appends them as nodes in pop order; after the
+ * scores in push order; -0 and +0 are equal) and appends them as nodes in pop
+ * order; after the
  * round every popped node of depth < L pushes its K children (the depth-(d+1)
  * list), in pop order, each node's children in list order.  With w = 1 this is
  * the plain best-first (priority-queue) construction, and the tree is the
