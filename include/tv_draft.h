@@ -70,9 +70,8 @@ tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, int64_t row
  * The candidate heap starts with the K depth-1 candidates (the roots); each
  * round pops the min(w, budget - n) best candidates (higher score first, equal
  * scores in push order; -0 and +0 are equal) and appends them as nodes in pop
- * order; after the
- * round every popped node of depth < L pushes its K children (the depth-(d+1)
- * list), in pop order, each node's children in list order.  With w = 1 this is
+ * order; after the round every popped node of depth < L pushes its K children
+ * (the depth-(d+1) list), in pop order, each node's children in list order.  With w = 1 this is
  * the plain best-first (priority-queue) construction, and the tree is the
  * `budget` best-scoring nodes of the K-ary tree of depth L.
  *
