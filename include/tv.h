@@ -19,7 +19,9 @@
  * Conventions shared by every call
  *   - Every pointer argument is DEVICE memory owned by the caller (for example
  *     allocated by PyTorch).  The library allocates nothing and keeps no
- *     pointer after the call returns.
+ *     pointer after the call returns, with one exception: tv_argmax_noalloc
+ *     keeps its partials in a fixed static device array of the library and
+ *     caches that array's device address per device (see its comment).
  *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL means the
  *     legacy default stream) and never synchronises with the host.
  *   - The return value reports argument/shape validation and launch errors
@@ -235,7 +237,9 @@ tv_status tv_argmax_sm(const void *logits, int dtype, int64_t rows, int64_t V,
  *
  * The first call made with a given device current looks up the array's device
  * address (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture.  Every call shares the one array and leaves its partials
+ * any stream capture.  The cached address belongs to the device's primary
+ * context: after cudaDeviceReset (or any other teardown of that context) it is
+ * stale, so this call must not be used again in that process.  Every call shares the one array and leaves its partials
  * behind (each call writes every partial it reads, so nothing needs clearing),
  * so calls that may overlap on the GPU -- on different streams without
  * ordering between them -- race and must not be issued.

@@ -77,7 +77,9 @@ typedef struct tv_step_args {
 /*
  * tv_verify_step -- enqueue one whole step on `stream` (eager launches).
  * Errors: those of the five calls (the first one that fails is returned and
- * nothing after it is enqueued); TV_ERR_ARG for num_layers < 1 or NULL layers.
+ * nothing after it is enqueued); TV_ERR_ARG for num_layers < 1, NULL layers,
+ * or ctx_len and ctx_len_out being the same array when num_layers > 1 (every
+ * layer's commit reads ctx_len after the first has written ctx_len_out).
  */
 tv_status tv_verify_step(const tv_step_args *a, tv_stream stream);
 

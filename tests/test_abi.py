@@ -133,6 +133,25 @@ def test_graph_host_argument_checks(lib):
     lib.tv_verify_graph_destroy(None)
 
 
+def test_graph_rejects_aliased_ctx_len(lib):
+    """Two layers whose commits share one ctx_len array for input and output
+    would commit the second layer's rows n_acc positions too far: rejected on
+    the host before anything is enqueued (no GPU needed)."""
+    from tree_speculative_decoding_build_gb300._lib import Layer, StepArgs
+    P = ctypes.c_void_p
+    lib.tv_verify_step.argtypes = [ctypes.POINTER(StepArgs), P]
+    lib.tv_verify_step.restype = ctypes.c_int
+    lib.tv_verify_graph_create.argtypes = [ctypes.POINTER(StepArgs), ctypes.POINTER(P)]
+    lib.tv_verify_graph_create.restype = ctypes.c_int
+    layers = (Layer * 2)()
+    a = StepArgs(B=1, N=8, Hq=4, Hkv=2, D=64, max_blocks=4, num_blocks=4, window_left=-1,
+                 num_layers=2, layers=layers)
+    a.ctx_len = a.ctx_len_out = P(0x1000)
+    assert lib.tv_verify_step(ctypes.byref(a), None) == 1
+    h = P()
+    assert lib.tv_verify_graph_create(ctypes.byref(a), ctypes.byref(h)) == 1 and not h.value
+
+
 def test_gdn_host_argument_checks(lib):
     P, I = ctypes.c_void_p, ctypes.c_int
     lib.tv_gdn_tree_verify.argtypes = [P] * 7 + [I] * 6 + [P] * 3 + [I, P, P]

@@ -23,8 +23,20 @@ struct tv_graph_s {
 namespace tv {
 namespace {
 
-tv_status enqueue_step(const tv_step_args *a, cudaStream_t s) {
+// Host checks of the step's own arguments (each call checks its own too).
+tv_status check_step(const tv_step_args *a) {
   if (!a || a->num_layers < 1 || !a->layers) return TV_ERR_ARG;
+  // every layer's commit reads ctx_len and writes ctx_len_out: one array for
+  // both would make layer 2 onward commit its rows n_acc positions too far
+  if (a->num_layers > 1 && a->ctx_len != nullptr &&
+      static_cast<const void *>(a->ctx_len) == static_cast<const void *>(a->ctx_len_out))
+    return TV_ERR_ARG;
+  return TV_OK;
+}
+
+tv_status enqueue_step(const tv_step_args *a, cudaStream_t s) {
+  const tv_status c = check_step(a);
+  if (c != TV_OK) return c;
   const tv_stream st = reinterpret_cast<tv_stream>(s);
   tv_status r = tv_build_ancestors(a->parent, a->depth, a->ctx_len, a->B, a->N, a->anc, a->pos,
                                    a->status, st);
@@ -100,7 +112,8 @@ extern "C" tv_status tv_verify_step(const tv_step_args *a, tv_stream stream) {
 extern "C" tv_status tv_verify_graph_create(const tv_step_args *a, tv_graph *out) {
   if (!out) return TV_ERR_ARG;
   *out = nullptr;
-  if (!a || a->num_layers < 1 || !a->layers) return TV_ERR_ARG;
+  const tv_status c = check_step(a);
+  if (c != TV_OK) return c;
   cudaStream_t cs = nullptr;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return TV_ERR_CUDA;
   tv_graph_s *g = new (std::nothrow) tv_graph_s;
