@@ -28,14 +28,19 @@
 //                window / ancestor mask, writes P_j as bf16 pairs to TMEM.  O is
 //                rescaled in TMEM only when the row max grows by more than 2^8
 //                (the final division by the running sum makes any reference
-//                max exact).  At the end of a (sequence, KV head) segment
-//                warpgroup 0 merges the two O's; it also writes Q into TMEM at
-//                each segment start.
+//                max exact).  At the end of a (sequence, KV head) segment the
+//                two warpgroups exchange (max, sum) and each merges half of the
+//                columns of O_0 and O_1; warpgroup 0 writes Q into TMEM at a
+//                segment start, warpgroup 1 loads the next segment's Q early.
 // TMEM (512 columns): S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448); Q [448,512).
 // Work balance: the (sequence, KV head, tile) list, ragged in sequence length,
 // is cut into equal contiguous ranges, one per CTA.  A (sequence, KV head)
-// pair that falls inside one range is written directly; a pair cut across
-// ranges leaves (max, sum, O) partials that a small combine kernel merges.
+// pair that falls inside one range is written directly.  A pair cut across
+// ranges leaves one (max, sum, O) partial per piece; each piece's CTA counts
+// itself in at the pair's counter, and the CTA whose piece completes the
+// count merges all of them into the output, inside this grid (no second
+// kernel: a merge grid after this one cost 8-10 us of dependent latency).  A
+// one-block grid launched just before zeroes the counters.
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // TV_ERR_CUDA in status[] and winds down.
 #include <cuda.h>
@@ -69,8 +74,9 @@ constexpr uint32_t kBlkBytes = 2 * kBlkChunk;          // one paged block: [2 ha
 constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffPre = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffCtx = kOffPre + 4 * (kMaxB + 1);
-constexpr uint32_t kOffMerge = (kOffCtx + 4 * kMaxB + 15) / 16 * 16;   // [2][128] float2
-constexpr uint32_t kSmemBytes = kOffMerge + 2 * kM * 8 + 1024;  // + alignment slack
+constexpr uint32_t kOffMerge = (kOffCtx + 4 * kMaxB + 15) / 16 * 16;   // [2 seg parity][2 wg][128] float2
+constexpr uint32_t kOffEpi = kOffMerge + 4 * kM * 8;   // [8 softmax warps][32 rows][64 B] output staging
+constexpr uint32_t kSmemBytes = kOffEpi + 8 * 2048 + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;     // S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448); Q [448,512)
 constexpr uint32_t kColO = 128;
 constexpr uint32_t kColP = 384;         // P as bf16 pairs: 64 keys = 32 columns
@@ -82,9 +88,13 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 struct TcParams {
   AttnParams a;
-  int *pre_out;       // [B+1] flat tile offsets, written by CTA 0 for the combine
-  float *part_o;      // [2*P][128][128]
-  float2 *part_ml;    // [2*P][128]
+  long long *lo_out;  // [P+1] first flat tile of every CTA's range (and the total)
+  longlong2 *desc;    // [P] the (sequence, KV head) pair CTA c starts and that runs
+                      // past its range: (first flat tile, end tile | pair << 32),
+                      // first = -1 when there is none
+  float *part_o;      // [2*P][128 dims][128 rows] unnormalised partial outputs,
+                      // dim-major so that a warp's 32 rows store 128 contiguous bytes
+  float2 *part_ml;    // [2*P][128]      (max, sum) of each partial
   int node_pad;       // N rounded up to 16
 };
 
@@ -182,6 +192,57 @@ struct Cursor {
   }
 };
 
+// Cut points of the work split.  CTA c's range starts at snap_cut(c T / P):
+// an even cut, moved to the nearest (sequence, KV head) pair boundary when one
+// lies within kSnap tiles.  A pair cut between CTAs costs a partial per piece,
+// an extra segment end and a merge, about as much as streaming kSnap tiles, so
+// short pairs (sliding windows, short contexts) are no longer cut at all.  The
+// function is monotone, so consecutive ranges meet.
+constexpr long long kSnap = 5;
+__device__ __forceinline__ long long snap_cut(const int *pre, int B, int Hkv, long long x) {
+  if (x <= 0 || x >= pre[B]) return x;
+  int lo = 0, up = B - 1;
+  while (lo < up) {  // largest b with pre[b] <= x
+    const int mid = (lo + up + 1) >> 1;
+    if (pre[mid] <= x) lo = mid;
+    else up = mid - 1;
+  }
+  const long long tiles = (pre[lo + 1] - pre[lo]) / Hkv;
+  const long long below = pre[lo] + (x - pre[lo]) / tiles * tiles, above = below + tiles;
+  const long long d_lo = x - below, d_hi = above - x;
+  if (d_lo <= d_hi) return d_lo <= kSnap ? below : x;
+  return d_hi <= kSnap ? above : x;
+}
+
+// One 32-dim chunk of the bf16 output of the 32 rows a warp owns (lane = row
+// 32 * quad + lane, its 32 values packed in pk): staged through the warp's own
+// 2 KB of shared memory (16-byte units XOR-swizzled by row, so neither the
+// writes nor the reads conflict), then stored so that four lanes write one
+// row's 64 contiguous bytes.  Row m = t * G + g goes to out + row_base +
+// (t * Hq + g) * 128 + col0; rows m >= R are not stored.
+__device__ __forceinline__ void stage_store_bf16(uint32_t stg, const uint32_t (&pk)[16], int lane,
+                                                 int quad, __nv_bfloat16 *out, size_t row_base,
+                                                 int Hq, int G, int R, int col0) {
+  const uint32_t f = (uint32_t)(lane >> 1) & 3u;
+#pragma unroll
+  for (uint32_t u = 0; u < 4; ++u)
+    st_shared_v4(stg + (uint32_t)lane * 64u + ((u ^ f) << 4), pk[4 * u], pk[4 * u + 1], pk[4 * u + 2],
+                 pk[4 * u + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint32_t u = (uint32_t)lane & 3u;
+    const uint4 v = ld_shared_v4(stg + (uint32_t)r * 64u + ((u ^ ((uint32_t)(r >> 1) & 3u)) << 4));
+    const int m = quad * 32 + r;
+    if (m < R) {
+      const int t = m / G, g = m - t * G;
+      *reinterpret_cast<uint4 *>(out + row_base + ((size_t)t * Hq + g) * kD + col0 + u * 8) = v;
+    }
+  }
+  __syncwarp();  // the staging buffer may be refilled
+}
+
 __device__ __forceinline__ int ctx_tiles(int ctx, int window_left) {
   const int blk_lo = first_visible_block(ctx, window_left);
   const int nblk = (ctx + kBlock - 1) / kBlock - blk_lo;
@@ -260,8 +321,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
       mbar_init(smem_u32(&bars.p_full[i]), 128);
       mbar_init(smem_u32(&bars.pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars.merge), 128);
-    mbar_init(smem_u32(&bars.o_free), 128);
+    mbar_init(smem_u32(&bars.merge), 256);
+    mbar_init(smem_u32(&bars.o_free), 256);
     mbar_init(smem_u32(&bars.fin), 1);
     fence_mbar_init();
   }
@@ -271,12 +332,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   const uint32_t tmem = s_tmem;
   const long long T = s_pre[B];
   const long long P = gridDim.x;
-  const long long lo = (long long)blockIdx.x * T / P;
-  const long long hi = (long long)(blockIdx.x + 1) * T / P;
-  if (blockIdx.x == 0)
-    for (int b = tid; b <= B; b += kThreads) tp.pre_out[b] = s_pre[b];
-  // Let the combine grid be scheduled as CTAs of this grid exit; it waits for
-  // this grid's completion (and memory) before it reads anything.
+  const long long lo = snap_cut(s_pre, B, Hkv, (long long)blockIdx.x * T / P);
+  const long long hi = snap_cut(s_pre, B, Hkv, (long long)(blockIdx.x + 1) * T / P);
+  if (tid == 0) {
+    tp.lo_out[blockIdx.x] = lo;
+    if (blockIdx.x + 1 == gridDim.x) tp.lo_out[gridDim.x] = hi;
+  }
+  // A grid launched after this one as a programmatic dependent may be
+  // scheduled as CTAs of this grid exit; it must wait for this grid's
+  // completion (griddepcontrol.wait) before reading its outputs.
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   volatile int *abort_flag = &s_abort;
 
@@ -600,7 +664,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
     long long seg_f0 = lo;
     bool seg_complete = false;
     bool q_next_loaded = false;  // Q of the coming segment already in TMEM
+    // the pair this CTA starts and that runs past its range (merged by the
+    // combine grid): its first flat tile, end tile and index b * Hkv + kvh
+    long long own_s = -1, own_e = 0;
+    int own_pair = 0;
     const uint32_t t_p = tlane + kColP + (uint32_t)x * 32;
+    const uint32_t stg = sbase + kOffEpi + (uint32_t)(warp - 2) * 2048u;  // this warp's staging
     while (cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
       if (cur.seg_start(lo)) {
@@ -749,119 +818,108 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
                                                  (uint32_t)((last_j >> 1) & 1), abort_flag));
           if (!ok) break;
         }
-        float2 *mrg = reinterpret_cast<float2 *>(smem + kOffMerge) + (seg & 1) * kM;
         // is there a next segment in this CTA's range (then warpgroup 1 loads
-        // its Q rows now)
+        // its Q rows into TMEM now, before the merge, so that the next
+        // segment's first S does not wait for the merge)
         const bool q_next = cur.f + 1 < hi && cur.b + (cur.kvh + 1 == p.Hkv ? 1 : 0) < B;
         q_next_loaded = q_next;
-        if (x == 1) {
-          // hand (max, sum) to warpgroup 0; wait until it consumed the previous
-          // segment's hand-over so the two never drift more than one apart
-          if (seg > 0) {
-            ok = __all_sync(0xffffffffu,
-                            wait_fast(smem_u32(&bars.o_free), (uint32_t)((seg - 1) & 1), abort_flag));
-            if (!ok) break;
-          }
-          mrg[m] = make_float2(m_used, l);
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bars.merge));
-          if (q_next) {
-            // while warpgroup 0 merges, the Q rows of the next segment of this
-            // CTA's range go into TMEM once this segment's last S has read the
-            // old ones (q_empty); that segment's start then skips the load
-            const int nb = cur.kvh + 1 < p.Hkv ? cur.b : cur.b + 1;
-            const int nk = cur.kvh + 1 < p.Hkv ? cur.kvh + 1 : 0;
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q + (((size_t)nb * N + t) * p.Hq + nk * G + g) * kD);
-            ok = __all_sync(0xffffffffu,
-                            wait_fast(smem_u32(&bars.q_empty), (uint32_t)(seg & 1), abort_flag));
-            if (!ok) break;
+        // both warpgroups hand over (running max, running sum) ...
+        float2 *mrg = reinterpret_cast<float2 *>(smem + kOffMerge) + (seg & 1) * 2 * kM;
+        mrg[x * kM + m] = make_float2(m_used, l);
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.merge));
+        if (x == 1 && q_next) {
+          // once this segment's last S has read the old Q rows (q_empty)
+          const int nb = cur.kvh + 1 < p.Hkv ? cur.b : cur.b + 1;
+          const int nk = cur.kvh + 1 < p.Hkv ? cur.kvh + 1 : 0;
+          const uint4 *src = reinterpret_cast<const uint4 *>(
+              p.q + (((size_t)nb * N + t) * p.Hq + nk * G + g) * kD);
+          ok = __all_sync(0xffffffffu,
+                          wait_fast(smem_u32(&bars.q_empty), (uint32_t)(seg & 1), abort_flag));
+          if (!ok) break;
 #pragma unroll 1
-            for (int hf = 0; hf < 2; ++hf) {  // 64 dims at a time
-              uint32_t qn[32];
+          for (int hf = 0; hf < 2; ++hf) {  // 64 dims at a time
+            uint32_t qn[32];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const uint4 w = row_ok ? __ldg(src + 8 * hf + v) : make_uint4(0, 0, 0, 0);
-                qn[v * 4 + 0] = w.x;
-                qn[v * 4 + 1] = w.y;
-                qn[v * 4 + 2] = w.z;
-                qn[v * 4 + 3] = w.w;
-              }
-              tmem_st32(tlane + kColQ + 32 * hf, qn);
+            for (int v = 0; v < 8; ++v) {
+              const uint4 w = row_ok ? __ldg(src + 8 * hf + v) : make_uint4(0, 0, 0, 0);
+              qn[v * 4 + 0] = w.x;
+              qn[v * 4 + 1] = w.y;
+              qn[v * 4 + 2] = w.z;
+              qn[v * 4 + 3] = w.w;
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(smem_u32(&bars.q_full));
+            tmem_st32(tlane + kColQ + 32 * hf, qn);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.q_full));
+        }
+        // ... then each merges its share of the 32-column chunks of O_0 and
+        // O_1: warpgroup 0 chunks 0-2, warpgroup 1 (which loaded Q) chunk 3
+        ok = __all_sync(0xffffffffu,
+                        wait_fast(smem_u32(&bars.merge), (uint32_t)(seg & 1), abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const float2 h0 = mrg[m], h1 = mrg[kM + m];
+        const float M = fmaxf(h0.x, h1.x);
+        const float w0 = h0.x == -INFINITY ? 0.f : ex2(h0.x - M);
+        const float w1 = h1.x == -INFINITY ? 0.f : ex2(h1.x - M);
+        const float L = h0.y * w0 + h1.y * w1;
+        const uint32_t t_o0 = tlane + kColO, t_o1 = tlane + kColO + kD;
+        const int c_lo = x == 0 ? 0 : 3, c_hi = x == 0 ? 3 : 4;
+        if (seg_complete) {
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          const float a0 = w0 * inv, a1 = w1 * inv;
+          const size_t row_base = ((size_t)b * N * p.Hq + (size_t)kvh * G) * kD;
+#pragma unroll 1
+          for (int c = c_lo; c < c_hi; ++c) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(t_o0 + c * 32, o0);
+            tmem_ld32(t_o1 + c * 32, o1);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float f0 = (w0 > 0.f ? __uint_as_float(o0[e]) * a0 : 0.f) +
+                               (w1 > 0.f ? __uint_as_float(o1[e]) * a1 : 0.f);
+              const float f1 = (w0 > 0.f ? __uint_as_float(o0[e + 1]) * a0 : 0.f) +
+                               (w1 > 0.f ? __uint_as_float(o1[e + 1]) * a1 : 0.f);
+              pk[e >> 1] = pack_bf16(f0, f1);
+            }
+            stage_store_bf16(stg, pk, lane, quad, p.out, row_base, p.Hq, G, R, c * 32);
           }
         } else {
-          ok = __all_sync(0xffffffffu,
-                          wait_fast(smem_u32(&bars.merge), (uint32_t)(seg & 1), abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          const float2 other = mrg[m];
-          const float M = fmaxf(m_used, other.x);
-          const float w0 = m_used == -INFINITY ? 0.f : ex2(m_used - M);
-          const float w1 = other.x == -INFINITY ? 0.f : ex2(other.x - M);
-          const float L = l * w0 + other.y * w1;
-          const uint32_t t_o0 = tlane + kColO, t_o1 = tlane + kColO + kD;
-          if (seg_complete) {
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            const float a0 = w0 * inv, a1 = w1 * inv;
-            __nv_bfloat16 *dst = p.out + (((size_t)b * N + t) * p.Hq + kvh * G + g) * kD;
+          const int slot = 2 * (int)blockIdx.x + (seg_f0 == lo ? 0 : 1);
+          float *dst = tp.part_o + (size_t)slot * kD * kM + m;  // dim-major: dim d at d * 128
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t o0[32], o1[32];
-              tmem_ld32(t_o0 + c * 32, o0);
-              tmem_ld32(t_o1 + c * 32, o1);
-              tmem_wait_ld();
-              if (row_ok) {
+          for (int c = c_lo; c < c_hi; ++c) {
+            uint32_t o0[32], o1[32];
+            tmem_ld32(t_o0 + c * 32, o0);
+            tmem_ld32(t_o1 + c * 32, o1);
+            tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; e += 8) {
-                  float v[8];
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) {
-                    const float f0 = w0 > 0.f ? __uint_as_float(o0[e + k]) * a0 : 0.f;
-                    const float f1 = w1 > 0.f ? __uint_as_float(o1[e + k]) * a1 : 0.f;
-                    v[k] = f0 + f1;
-                  }
-                  uint4 w;
-                  w.x = pack_bf16(v[0], v[1]);
-                  w.y = pack_bf16(v[2], v[3]);
-                  w.z = pack_bf16(v[4], v[5]);
-                  w.w = pack_bf16(v[6], v[7]);
-                  *reinterpret_cast<uint4 *>(dst + c * 32 + e) = w;
-                }
-              }
-            }
-          } else {
-            const int slot = 2 * (int)blockIdx.x + (seg_f0 == lo ? 0 : 1);
-            float *dst = tp.part_o + ((size_t)slot * kM + m) * kD;
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t o0[32], o1[32];
-              tmem_ld32(t_o0 + c * 32, o0);
-              tmem_ld32(t_o1 + c * 32, o1);
-              tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; e += 4) {
-                float4 v;
-                v.x = (w0 > 0.f ? __uint_as_float(o0[e]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e]) * w1 : 0.f);
-                v.y = (w0 > 0.f ? __uint_as_float(o0[e + 1]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 1]) * w1 : 0.f);
-                v.z = (w0 > 0.f ? __uint_as_float(o0[e + 2]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 2]) * w1 : 0.f);
-                v.w = (w0 > 0.f ? __uint_as_float(o0[e + 3]) * w0 : 0.f) + (w1 > 0.f ? __uint_as_float(o1[e + 3]) * w1 : 0.f);
-                *reinterpret_cast<float4 *>(dst + c * 32 + e) = v;
-              }
-            }
-            tp.part_ml[(size_t)slot * kM + m] = make_float2(M, L);
+            for (int e = 0; e < 32; ++e)
+              dst[(size_t)(c * 32 + e) * kM] = (w0 > 0.f ? __uint_as_float(o0[e]) * w0 : 0.f) +
+                                               (w1 > 0.f ? __uint_as_float(o1[e]) * w1 : 0.f);
           }
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bars.o_free));
+          if (x == 0) tp.part_ml[(size_t)slot * kM + m] = make_float2(M, L);
+          if (seg_f0 == cur.f - cur.u) {  // the piece holds the pair's first tile
+            own_s = seg_f0;
+            own_e = seg_f0 + cur.tiles;
+            own_pair = b * p.Hkv + kvh;
+          }
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.o_free));  // O_0 and O_1 may be overwritten
         ++seg;
       }
       ++j;
       cur.next();
     }
+    // every CTA writes its descriptor (the workspace is not cleared between
+    // calls); the combine grid reads it once this grid has completed
+    if (warp == 2 && lane == 0)
+      tp.desc[blockIdx.x] = make_longlong2(own_s, own_s < 0 ? 0 : (own_e | ((long long)own_pair << 32)));
     if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
   }
 
@@ -873,98 +931,70 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   }
 }
 
-// Merge the partials of every (sequence, KV head) pair whose tiles were split
-// across CTAs.  Blocks (c-1, y) with 1 <= c < P own the pair that CTA c-1
-// started and that runs past CTA c-1's range: the pair holding CTA c-1's last
-// flat tile.  Every split pair has exactly one such c; the other blocks exit
-// after one look at the tile offsets (staged in shared memory).  Block row y
-// takes output rows 32y .. 32y+31, four per warp (their loads issued
-// together); lane l owns dims 4l .. 4l+3.  Launched as a programmatic
-// dependent of the attention grid: it waits for that grid before any read.
-constexpr int kCombRows = 4;  // rows per warp
-__global__ void __launch_bounds__(256, 4) attn_tc_combine_kernel(const TcParams tp, int P) {
+// Merge the partials of the pairs cut between CTAs.  Block (c, y) takes the
+// pair CTA c starts and that runs past its range (CTA c's descriptor; most
+// blocks find none and exit) and its dims 64y .. 64y+63: thread i owns row
+// i % 128 and 32 dims.  The pieces are in CTAs c, c+1, ... up to the one whose
+// range holds the pair's last tile; slot 2d (a piece that starts a CTA's
+// range) or 2c + 1 (CTA c's piece, when the pair starts inside its range).
+// Launched as a programmatic dependent of the attention grid: it waits for
+// that grid's completion before any read.
+__global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp, int P) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const AttnParams &p = tp.a;
-  __shared__ int s_pre[kMaxB + 1];
-  for (int i = threadIdx.x; i <= p.B; i += blockDim.x) s_pre[i] = tp.pre_out[i];
-  __syncthreads();
-  const int c = blockIdx.x + 1;
-  const int m0 = blockIdx.y * (8 * kCombRows) + (threadIdx.x >> 5) * kCombRows;
-  const long long T = s_pre[p.B];
-  const long long loc = (long long)c * T / P;
-  if (loc == 0 || loc >= T || m0 >= p.R) return;
-  const long long f = loc - 1;  // last tile of CTA c-1 (when that range is non-empty)
-  // sequence b with s_pre[b] <= f < s_pre[b+1]
-  int lo = 0, hi = p.B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (s_pre[mid] <= f) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int tiles = (s_pre[b + 1] - s_pre[b]) / p.Hkv;
-  const int kvh = (int)((f - s_pre[b]) / tiles);
-  const long long S = s_pre[b] + (long long)kvh * tiles, E = S + tiles;
-  auto cta_of = [&](long long x) { return (int)(((x + 1) * P + T - 1) / T - 1); };
-  const int c0 = cta_of(S), c1 = cta_of(E - 1);
-  if (c0 != c - 1 || c1 == c0) return;
-  const int lane = threadIdx.x & 31;
-  // CTA d covers flat tiles [d*T/P, (d+1)*T/P); ranges can be empty when T < P
-  auto slot_of = [&](int d) {
-    const long long ld = (long long)d * T / P;
-    if (ld == (long long)(d + 1) * T / P) return -1;
-    return 2 * d + ((d == c0 && ld < S) ? 1 : 0);
-  };
-  float M[kCombRows];
+  const int c = blockIdx.x;
+  const longlong2 dsc = tp.desc[c];
+  if (dsc.x < 0) return;
+  const long long S = dsc.x, E = dsc.y & 0xffffffffll;
+  const int pair = (int)(dsc.y >> 32);
+  const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
+  __shared__ long long s_lo[33];
+  const int m = threadIdx.x & 127, d0 = 64 * blockIdx.y + 32 * (threadIdx.x >> 7);
+  float Mx = -INFINITY, Lx = 0.f, acc[32];
 #pragma unroll
-  for (int i = 0; i < kCombRows; ++i) M[i] = -INFINITY;
-  for (int d = c0; d <= c1; ++d) {
-    const int slot = slot_of(d);
-    if (slot < 0) continue;
-#pragma unroll
-    for (int i = 0; i < kCombRows; ++i)
-      if (m0 + i < p.R) M[i] = fmaxf(M[i], tp.part_ml[(size_t)slot * kM + m0 + i].x);
-  }
-  float L[kCombRows];
-  float4 acc[kCombRows];
-#pragma unroll
-  for (int i = 0; i < kCombRows; ++i) {
-    L[i] = 0.f;
-    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int d = c0; d <= c1; ++d) {
-    const int slot = slot_of(d);
-    if (slot < 0) continue;
-    float2 ml[kCombRows];
-    float4 o[kCombRows];
-#pragma unroll
-    for (int i = 0; i < kCombRows; ++i) {
-      if (m0 + i < p.R) {
-        ml[i] = tp.part_ml[(size_t)slot * kM + m0 + i];
-        o[i] = *reinterpret_cast<const float4 *>(tp.part_o + ((size_t)slot * kM + m0 + i) * kD + lane * 4);
+  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+  // windows of 32 CTAs: their range starts, then the pieces they hold
+  for (int w0 = c; w0 < P; w0 += 32) {
+    __syncthreads();
+    if (threadIdx.x < 33) s_lo[threadIdx.x] = w0 + (int)threadIdx.x <= P ? tp.lo_out[w0 + threadIdx.x] : E;
+    __syncthreads();
+    bool done = false;
+    for (int i = 0; i < 32 && w0 + i < P; ++i) {
+      const int d = w0 + i;
+      const long long ld = s_lo[i], hd = s_lo[i + 1];
+      if (ld >= E) {
+        done = true;
+        break;
       }
-    }
+      if (ld == hd) continue;  // an empty range holds no piece
+      const int slot = 2 * d + ((d == c && ld < S) ? 1 : 0);
+      const float2 ml = __ldcg(tp.part_ml + (size_t)slot * kM + m);
+      const float *src = tp.part_o + ((size_t)slot * kD + d0) * kM + m;
+      float o[32];
 #pragma unroll
-    for (int i = 0; i < kCombRows; ++i) {
-      if (m0 + i >= p.R || ml[i].x == -INFINITY) continue;
-      const float w = exp2f(ml[i].x - M[i]);
-      L[i] += ml[i].y * w;
-      acc[i].x += o[i].x * w;
-      acc[i].y += o[i].y * w;
-      acc[i].z += o[i].z * w;
-      acc[i].w += o[i].w * w;
+      for (int k = 0; k < 32; ++k) o[k] = __ldcg(src + (size_t)k * kM);
+      if (ml.x == -INFINITY) continue;  // no key seen: O = 0
+      const float Mn = fmaxf(Mx, ml.x);
+      const float a = Mx == -INFINITY ? 0.f : exp2f(Mx - Mn), w = exp2f(ml.x - Mn);
+      Lx = Lx * a + ml.y * w;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[k] = acc[k] * a + o[k] * w;
+      Mx = Mn;
     }
+    if (done) break;
   }
+  if (m >= p.R) return;
+  const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+  const int t = m / p.G, g = m - t * p.G;
+  __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * kD + d0;
 #pragma unroll
-  for (int i = 0; i < kCombRows; ++i) {
-    const int m = m0 + i;
-    if (m >= p.R) break;
-    const float inv = L[i] > 0.f ? 1.f / L[i] : 0.f;
-    const int t = m / p.G, g = m - t * p.G;
-    __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * kD + lane * 4;
-    uint2 w;
-    w.x = pack_bf16(acc[i].x * inv, acc[i].y * inv);
-    w.y = pack_bf16(acc[i].z * inv, acc[i].w * inv);
-    *reinterpret_cast<uint2 *>(dst) = w;
+  for (int e = 0; e < 32; e += 8) {
+    uint4 v;
+    v.x = pack_bf16(acc[e] * inv, acc[e + 1] * inv);
+    v.y = pack_bf16(acc[e + 2] * inv, acc[e + 3] * inv);
+    v.z = pack_bf16(acc[e + 4] * inv, acc[e + 5] * inv);
+    v.w = pack_bf16(acc[e + 6] * inv, acc[e + 7] * inv);
+    *reinterpret_cast<uint4 *>(dst + e) = v;
   }
 }
 
@@ -1004,10 +1034,12 @@ bool attention_tc_supported(const AttnParams &p) {
 }
 
 size_t attention_tc_workspace(int B, int P) {
-  const size_t pre = ((size_t)(B + 1) * sizeof(int) + 255) / 256 * 256;
+  (void)B;
+  const size_t lo = ((size_t)(P + 1) * sizeof(long long) + 255) / 256 * 256;
+  const size_t desc = ((size_t)P * sizeof(longlong2) + 255) / 256 * 256;
   const size_t ml = ((size_t)2 * P * kM * sizeof(float2) + 255) / 256 * 256;
   const size_t o = (size_t)2 * P * kM * kD * sizeof(float);
-  return pre + ml + o;
+  return lo + desc + ml + o;
 }
 
 cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream_t stream) {
@@ -1015,8 +1047,10 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   TcParams tp{};
   tp.a = a;
   char *ws = static_cast<char *>(workspace);
-  tp.pre_out = reinterpret_cast<int *>(ws);
-  ws += ((size_t)(a.B + 1) * sizeof(int) + 255) / 256 * 256;
+  tp.lo_out = reinterpret_cast<long long *>(ws);
+  ws += ((size_t)(P + 1) * sizeof(long long) + 255) / 256 * 256;
+  tp.desc = reinterpret_cast<longlong2 *>(ws);
+  ws += ((size_t)P * sizeof(longlong2) + 255) / 256 * 256;
   tp.part_ml = reinterpret_cast<float2 *>(ws);
   ws += ((size_t)2 * P * kM * sizeof(float2) + 255) / 256 * 256;
   tp.part_o = reinterpret_cast<float *>(ws);
@@ -1061,7 +1095,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   if (e != cudaSuccess) return e;
   if (P > 1) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P - 1, (a.R + 8 * kCombRows - 1) / (8 * kCombRows));
+    cfg.gridDim = dim3(P, 2);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
