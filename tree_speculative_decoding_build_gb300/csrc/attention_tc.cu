@@ -34,13 +34,19 @@
 //                segment start, warpgroup 1 loads the next segment's Q early.
 // TMEM (512 columns): S0, S1 [0,128); O0, O1 [128,384); P0, P1 [384,448); Q [448,512).
 // Work balance: the (sequence, KV head, tile) list, ragged in sequence length,
-// is cut into equal contiguous ranges, one per CTA.  A (sequence, KV head)
-// pair that falls inside one range is written directly.  A pair cut across
-// ranges leaves one (max, sum, O) partial per piece; each piece's CTA counts
-// itself in at the pair's counter, and the CTA whose piece completes the
-// count merges all of them into the output, inside this grid (no second
-// kernel: a merge grid after this one cost 8-10 us of dependent latency).  A
-// one-block grid launched just before zeroes the counters.
+// is cut into equal contiguous ranges, one per CTA, each cut moved to a pair
+// boundary when one lies within a few tiles.  A (sequence, KV head) pair that
+// falls inside one range is written directly.  A pair cut across ranges leaves
+// one (max, sum, O) partial per piece, merged by attn_tc_combine_kernel.
+// Programmatic dependent launch: this grid may start while the kernel before
+// it on the stream finishes (the ancestor kernel, or the previous layer's
+// combine grid), so its prologue, block-id loads and first K/V copies overlap
+// that kernel.  Everything read before griddepcontrol.wait is an
+// input no earlier kernel of a verify step writes (context lengths, block
+// tables, Q, K/V); ancestor masks and positions are read, and status words
+// and the scratch (range starts, descriptors, partials) written, only after
+// it.  Data errors found before it are kept in a shared-memory bitmap and
+// written to status[] at the end.
 // Every mbarrier wait is bounded in time; on expiry the kernel records
 // TV_ERR_CUDA in status[] and winds down.
 #include <cuda.h>
@@ -243,6 +249,10 @@ __device__ __forceinline__ void stage_store_bf16(uint32_t stg, const uint32_t (&
   __syncwarp();  // the staging buffer may be refilled
 }
 
+// Programmatic dependent launch: wait until the kernels this grid depends on
+// have completed and their writes are visible (returns at once otherwise).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ int ctx_tiles(int ctx, int window_left) {
   const int blk_lo = first_visible_block(ctx, window_left);
   const int nblk = (ctx + kBlock - 1) / kBlock - blk_lo;
@@ -261,6 +271,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   __shared__ Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ uint32_t s_bad[kMaxB / 32];  // sequences with a bad block id or context length
 
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -272,11 +283,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   const int NP = tp.node_pad;
 
   // ---- schedule: context tiles per sequence, prefix over (sequence, KV head)
+  for (int i = tid; i < kMaxB / 32; i += kThreads) s_bad[i] = 0;
+  __syncthreads();
   for (int b = tid; b < B; b += kThreads) {
     int ctx = p.ctx_len[b];
     const int cap = p.max_blocks * kBlock;
     if (ctx < 0 || ctx > cap) {
-      if (blockIdx.x == 0) set_status(p.status, b, TV_ERR_BLOCK);
+      if (blockIdx.x == 0) atomicOr(&s_bad[b >> 5], 1u << (b & 31));
       ctx = ctx < 0 ? 0 : cap;
     }
     s_ctx[b] = ctx;
@@ -334,10 +347,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   const long long P = gridDim.x;
   const long long lo = snap_cut(s_pre, B, Hkv, (long long)blockIdx.x * T / P);
   const long long hi = snap_cut(s_pre, B, Hkv, (long long)(blockIdx.x + 1) * T / P);
-  if (tid == 0) {
-    tp.lo_out[blockIdx.x] = lo;
-    if (blockIdx.x + 1 == gridDim.x) tp.lo_out[gridDim.x] = hi;
-  }
   // A grid launched after this one as a programmatic dependent may be
   // scheduled as CTAs of this grid exit; it must wait for this grid's
   // completion (griddepcontrol.wait) before reading its outputs.
@@ -430,7 +439,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           r = r < 0 ? 0 : (r > kBlock ? kBlock : r);
           int id = __shfl_sync(0xffffffffu, cur_id, slot - win_base);
           if (r > 0 && (id < 0 || id >= p.num_blocks)) {
-            if (lane == 0) set_status(p.status, b, TV_ERR_BLOCK);
+            if (lane == 0) atomicOr(&s_bad[b >> 5], 1u << (b & 31));
             r = 0;
           }
           ids[i] = id;
@@ -509,8 +518,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
       int dummy = 0;
       for (int k = j > kStages ? j - kStages : 0; k < j; ++k)
         if ((k & 1) == par) wait_bar(smem_u32(&bars.kv_full[k % kStages]), (uint32_t)((k / kStages) & 1), &dummy);
+      grid_dep_wait();
       set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
     }
+
   } else if (warp == 1) {
     // ======================================================== MMA issuer
     // The only warp that issues tcgen05.mma (one lane per instruction, chosen
@@ -636,10 +647,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
       umma_commit_warp(smem_u32(&bars.fin));
       int dummy = 0;
       wait_bar(smem_u32(&bars.fin), 0, &dummy);
-      if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
+      if (!ok && lane == 0) {
+        grid_dep_wait();
+        set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
+      }
     }
   } else {
     // ======================================================== softmax / epilogue
+    // Masks and positions come from the ancestor kernel, and the scratch may
+    // still be read by the previous launch's combine grid: wait for them here
+    // (the producers and the MMA warp meanwhile fill the K/V stages).  A wait
+    // inside the tile loop instead measurably slowed the loop's code.
+    grid_dep_wait();
     // Two warpgroups take alternate tiles (x = parity of the CTA-wide tile
     // counter), each with its own running max / sum and its own O accumulator
     // in TMEM; at the end of a (sequence, KV head) segment warpgroup 0 merges
@@ -916,10 +935,14 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
       ++j;
       cur.next();
     }
-    // every CTA writes its descriptor (the workspace is not cleared between
-    // calls); the combine grid reads it once this grid has completed
-    if (warp == 2 && lane == 0)
+    // every CTA writes its range start and descriptor (the workspace is not
+    // cleared between calls); the combine grid reads them once this grid has
+    // completed
+    if (warp == 2 && lane == 0) {
+      tp.lo_out[blockIdx.x] = lo;
+      if (blockIdx.x + 1 == gridDim.x) tp.lo_out[gridDim.x] = hi;
       tp.desc[blockIdx.x] = make_longlong2(own_s, own_s < 0 ? 0 : (own_e | ((long long)own_pair << 32)));
+    }
     if (!ok && lane == 0) set_status(p.status, cur.valid() ? cur.b : 0, TV_ERR_CUDA);
   }
 
@@ -928,6 +951,18 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  } else if (warp == 0) {
+    // the data errors every warp of this CTA found, once the ancestor kernel
+    // has initialised the status words
+    grid_dep_wait();
+    for (int i = lane; i < (B + 31) / 32; i += 32) {
+      uint32_t bits = s_bad[i];
+      while (bits) {
+        const int bit = __ffs(bits) - 1;
+        bits &= bits - 1;
+        set_status(p.status, 32 * i + bit, TV_ERR_BLOCK);
+      }
+    }
   }
 }
 
@@ -940,7 +975,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
 // Launched as a programmatic dependent of the attention grid: it waits for
 // that grid's completion before any read.
 __global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp, int P) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next attention launch may start now: it waits for this grid before it
+  // touches the scratch read here
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  grid_dep_wait();
   const AttnParams &p = tp.a;
   const int c = blockIdx.x;
   const longlong2 dsc = tp.desc[c];
@@ -1090,20 +1128,25 @@ cudaError_t launch_attention_tc(const AttnParams &a, void *workspace, cudaStream
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<P, kThreads, kSmemBytes, stream>>>(mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
-  e = cudaGetLastError();
+  // both grids are programmatic dependents of the kernel before them on the
+  // stream: each may start while it finishes, and waits for it
+  // (griddepcontrol.wait) before touching what it may write
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_tc_kernel, mkc, mvc, mkcr, mvcr, mkt, mvt, tp);
   if (e != cudaSuccess) return e;
   if (P > 1) {
-    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P, 2);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, attn_tc_combine_kernel, tp, (int)P);
     if (e != cudaSuccess) return e;
   }

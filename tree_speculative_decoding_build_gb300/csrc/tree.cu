@@ -41,6 +41,9 @@ __global__ void build_ancestors_kernel(const int32_t *__restrict__ parent,
                                        const int32_t *__restrict__ ctx_len, int B, int N,
                                        uint64_t *__restrict__ anc, int32_t *__restrict__ pos,
                                        int32_t *__restrict__ status) {
+  // the tree-attention grids launched after this one may start at once: they
+  // wait for this grid's completion before reading anc / pos / status
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
