@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default="stress")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="only the workload's own measurements (no overlapped, draft or graph lines)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiling)")
     ap.add_argument("--path", choices=["verify", "draft", "graph", "gdn"], default="verify",
@@ -187,22 +189,27 @@ def recorded_traffic(workload="stress", batch=None, window_left=None):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons, sampled every ``period_ms`` from a
+    background thread.  Every sample carries the host time it arrived, so any
+    window of the run (the whole measurement, the timed loop, the sustained
+    loop) can be summarised afterwards."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_ms=100):
         self.gpu = gpu_index
-        self.lines = []
+        self.period_ms = period_ms
+        self.samples = []   # (host time, sm MHz, max MHz, power W, set of active reasons)
         self.proc = None
 
     def start(self, timeout=5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -210,45 +217,170 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         t0 = time.time()
-        while not self.lines and time.time() - t0 < timeout:
+        while not self.samples and time.time() - t0 < timeout:
             time.sleep(0.02)
-        self.lines.clear()
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            try:
+                pw = float(parts[3])
+            except ValueError:
+                pw = None
+            active = {n for n, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"}
+            self.samples.append((time.time(), sm, mx, pw, active))
 
     def stop(self):
         if self.proc is None:
-            return None
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in list(self.lines):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+
+    def summary(self, t0, t1, window):
+        """Median SM clock, the maximum, the samples and every throttle reason
+        seen between host times t0 and t1 (widened by one sampling period on
+        each side when no sample fell inside)."""
+        sel = [s for s in list(self.samples) if t0 <= s[0] <= t1]
+        if not sel:
+            pad = self.period_ms / 1000.0
+            sel = [s for s in list(self.samples) if t0 - pad <= s[0] <= t1 + pad]
+        if not sel:
             return None
-        sm.sort()
-        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        sm = sorted(s[1] for s in sel)
+        pw = [s[3] for s in sel if s[3] is not None]
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(s[2] for s in sel),
+                "samples": len(sel), "reasons": sorted(set().union(*(s[4] for s in sel))),
+                "power_w_max": max(pw) if pw else None, "window": window,
+                "window_s": round(t1 - t0, 3)}
 
 
-def workload_config(name, B=None, window_left=None):
-    """The workload, described from its specification (both arms use this)."""
+def l2_bytes(dev):
+    import torch
+    try:
+        return int(torch.cuda.get_device_properties(dev).L2_cache_size)
+    except Exception:
+        return 126 << 20
+
+
+class L2Flush:
+    """A read of twice the L2 size: nothing a timed launch reads stays cached.
+    A read rather than a write, so that no dirty lines are left for the timed
+    launch to write back."""
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.ones(2 * l2_bytes(dev) // 4, dtype=torch.int32, device=dev)
+        self.out = torch.empty((), dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        import torch
+        torch.amax(self.buf, dim=0, out=self.out)
+
+
+def capture(fn, reps, dev):
+    """A CUDA graph holding ``reps`` calls of fn() (the library's calls enqueue on
+    the current stream, which is the capture stream here)."""
+    import torch
+    fn()  # first call outside capture: one-time host set-up (function attributes)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        for _ in range(reps):
+            fn()
+    torch.cuda.synchronize(dev)
+    return g
+
+
+def graph_device_ms(fn, dev, iters, flush=None, reps=1):
+    """Device milliseconds per fn() call, from CUDA-graph replays timed with
+    CUDA events on the replay stream.  With ``flush`` every replay (one call)
+    is preceded by an L2 flush outside its event pair, and the events are
+    enqueued while the flush runs, so the GPU never waits on the host inside
+    a pair; without, ``reps`` calls are captured into one graph and replayed
+    back to back."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    g = capture(fn, 1 if flush else reps, dev)
+    for _ in range(3):
+        if flush:
+            flush()
+        g.replay()
+    torch.cuda.synchronize(dev)
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(iters)]
+        for e0, e1 in evs:
+            flush()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / iters
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / (iters * reps)
+    del g
+    return ms
+
+
+def h2d_link(nbytes, dev, streams=4, reps=5):
+    """Host-to-device copy rate from pinned memory for an upload of ``nbytes``:
+    one cudaMemcpyAsync, and the same bytes cut into one chunk per copy stream."""
+    import torch
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    css = [torch.cuda.Stream(device=dev) for _ in range(streams)]
+
+    def one():
+        dst.copy_(src, non_blocking=True)
+
+    def chunked():
+        done = []
+        for c, cs in enumerate(css):
+            cs.wait_stream(stream)
+            lo, hi = nbytes * c // streams, nbytes * (c + 1) // streams
+            with torch.cuda.stream(cs):
+                dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            done.append(ev)
+        for ev in done:
+            stream.wait_event(ev)
+
+    out = {}
+    for name, fn in (("single_copy_gbs", one), (f"{streams}_streams_gbs", chunked)):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out[name] = nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    return out
+
+
+def workload_config(name, B=None, window_left=None, l2=None):
+    """The workload, described from its specification (both arms use this);
+    ``l2`` is the line's statement of how L2 was handled between timed steps."""
     import workloads
     w = workloads.get(name)
     B = w.B if B is None else B
@@ -260,7 +392,7 @@ def workload_config(name, B=None, window_left=None):
                      f"block 16{', shuffled block tables' if w.shuffle_blocks else ''}, "
                      f"V={w.V} {w.logits_dtype} logits"),
         "batch": B, "tree_nodes": w.N, "ctx_len": ctx, "window_left": w.window_left,
-        "l2": "inputs larger than L2 (KV cache read per step >> 129 MB)",
+        "l2": l2,
     }
 
 
@@ -276,15 +408,25 @@ def attention_algorithmic_bytes(inp):
     return kv + q + tree_kv + out + table
 
 
+def step_working_set(inp, alg):
+    """Bytes one verify step reads from memory: the attention's algorithmic
+    bytes plus the logits (the rest is a few MB at most)."""
+    return alg + inp["logits"].numel() * inp["logits"].element_size()
+
+
 def bench_ours(args, rank, world, local):
+    import math
     import torch
     import torch.distributed as dist
     import workloads
     import tree_speculative_decoding_build_gb300 as tv
-    from tree_speculative_decoding_build_gb300 import _lib
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    if rank == 0:
+        sampler.start()
+    t_run0 = time.time()
     inp = workloads.make(args.workload, dev, seed=rank_seed(args.workload, rank), B=args.batch,
                          window_left=args.window_left)
     step = tv.VerifyStep(inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"],
@@ -294,6 +436,15 @@ def bench_ours(args, rank, world, local):
     for _ in range(max(3, args.warmup)):
         step(inp)
     torch.cuda.synchronize(dev)
+    eager_ms = None
+    if rank == 0:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            step(inp)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        eager_ms = e0.elapsed_time(e1) / 5
 
     # kernels launched per step: fixed by the launch plan
     ws_attn = tv.tv_tree_attention_workspace_size(inp["B"], inp["N"], inp["Hq"], inp["Hkv"],
@@ -301,51 +452,76 @@ def bench_ours(args, rank, world, local):
     dt = tv.TV_F32 if inp["logits_dtype"] == "f32" else tv.TV_BF16
     ws_arg = tv.tv_argmax_workspace_size(inp["B"] * inp["N"], inp["V"], dt)
     launches_per_step = 5 + (1 if ws_attn else 0) + (1 if ws_arg else 0)
+    alg = attention_algorithmic_bytes(inp)
+    l2 = l2_bytes(dev)
+    ws_bytes = step_working_set(inp, alg)
+    flush = L2Flush(dev)
+    per_step_flush = ws_bytes <= 2 * l2
 
-    # attention timed separately with events around its call, same stream
+    # the timed region: K replays of a CUDA graph holding one whole verify step
+    # (the same five calls through the binding); back to back when a step reads
+    # more than twice the L2, else each replay after an L2 flush
+    K = args.steps
+    g_step = capture(lambda: step(inp), 1, dev)
+    for _ in range(3):
+        g_step.replay()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_loop0 = time.time()
+    if per_step_flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for e0, e1 in evs:
+            flush()
+            e0.record(stream)
+            g_step.replay()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs)
+    else:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(K):
+            g_step.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = t0.elapsed_time(t1)
+    t_loop1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks(ms, world, dev)
+    status_ok = bool((step.out.status == 0).all().item())
+
+    # sustained: the same replays for at least a second, with their own clock record
+    n_sus = max(1, int(math.ceil(1000.0 / max(ms / K, 1e-3))))
+    t_sus0 = time.time()
+    s0 = torch.cuda.Event(enable_timing=True)
+    s1 = torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_sus):
+        if per_step_flush:
+            flush()
+        g_step.replay()
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_sus1 = time.time()
+    sus_ms = s0.elapsed_time(s1) / n_sus
+    del g_step
+
+    # tv_tree_attention alone (its two launches), L2 flushed before every launch
     o = step.out
-    B, N = inp["B"], inp["N"]
 
-    def run_step(ev_pair=None):
-        tv.tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], o.anc, o.pos, o.status)
-        if ev_pair is not None:
-            ev_pair[0].record(stream)
+    def attn():
         tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"],
                              inp["v_cache"], inp["block_table"], inp["ctx_len"], o.pos, o.anc,
                              o.attn, o.status, window_left=inp["window_left"],
                              workspace=step.ws_attn)
-        if ev_pair is not None:
-            ev_pair[1].record(stream)
-        tv.tv_argmax(inp["logits"].view(B * N, -1), o.argmax.view(B * N), step.ws_arg)
-        tv.tv_tree_walk(inp["tokens"], inp["parent"], o.argmax, inp["root_pred"], o.status,
-                        o.out_tokens, o.n_emit, o.acc_nodes, o.n_acc)
-        tv.tv_commit_kv(inp["k_tree"], inp["v_tree"], o.acc_nodes, o.n_acc, inp["ctx_len"],
-                        inp["block_table"], inp["k_cache"], inp["v_cache"], o.ctx_len_out,
-                        o.status)
-
-    K = args.steps
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    if rank == 0:
-        sampler.start()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for k in range(K):
-        run_step(attn_ev[k])
-    t1.record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    clocks = sampler.stop() if rank == 0 else None
-    ms = t0.elapsed_time(t1)
-    attn_ms = sum(a.elapsed_time(b) for a, b in attn_ev) / K
-    ms = max_over_ranks(ms, world, dev)
-    status_ok = bool((o.status == 0).all().item())
+    attn_iters = max(20, min(K, 300))
+    attn_ms = graph_device_ms(attn, dev, attn_iters, flush=flush)
+    attn_warm_ms = graph_device_ms(attn, dev, max(5, attn_iters // 10), reps=10)
 
     # end to end through the public API: pinned host inputs in, tokens out
     host_keys = ["tokens", "parent", "depth", "ctx_len", "root_pred", "block_table", "q",
@@ -360,12 +536,19 @@ def bench_ours(args, rank, world, local):
     e2e_ms = pipelined_e2e(lambda d: step(d), host, bufs, results, max(1, args.e2e_steps),
                            stream, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    link = h2d_link(h2d, dev) if rank == 0 else None
+    t_run1 = time.time()
 
     if rank != 0:
         return None
+    sampler.stop()
     peak, peak_kind = peaks()
-    alg = attention_algorithmic_bytes(inp)
     achieved = alg / (attn_ms * 1e-3) / 1e9
+    l2_note = (f"{'every replay after an L2 flush: ' if per_step_flush else ''}"
+               f"a step reads {ws_bytes / 1e6:.0f} MB (attention {alg / 1e6:.0f} MB + logits), "
+               f"L2 {l2 / 1e6:.0f} MB; the attention roofline launches each follow an L2 flush")
+    e2e_value = job_throughput(world, 1, e2e_ms)
+    link_peak = max(link.values()) if link else None
     line = {
         "metric": METRIC,
         "value": job_throughput(world, K, ms),
@@ -380,21 +563,37 @@ def bench_ours(args, rank, world, local):
         "dtype": "bf16",
         "data": "synthetic",
         "impl": "ours",
-        "config": workload_config(args.workload, args.batch, args.window_left),
-        "attention": {"ms": attn_ms, "kv_gbs": achieved, "algorithmic_bytes": alg,
-                      "frac_of_8tbs_nominal": achieved / 8000.0,
-                      "frac_of_peak": achieved / peak, "peak_kind": peak_kind},
+        "config": workload_config(args.workload, args.batch, args.window_left, l2=l2_note),
+        "timing": ("device: CUDA events around CUDA-graph replays of one whole verify step "
+                   "(tv_build_ancestors, tv_tree_attention, tv_argmax, tv_tree_walk, "
+                   "tv_commit_kv through the binding)"),
+        "eager_ms_per_step": eager_ms,
+        "attention": {"ms": attn_ms, "warm_ms": attn_warm_ms, "kv_gbs": achieved,
+                      "algorithmic_bytes": alg, "frac_of_8tbs_nominal": achieved / 8000.0,
+                      "frac_of_peak": achieved / peak, "peak_kind": peak_kind,
+                      "timing": (f"CUDA events around {attn_iters} graph replays of one "
+                                 "tv_tree_attention call (its counter-clearing and attention "
+                                 "kernels), each after an L2 flush; warm_ms: 10 calls per "
+                                 "replay, back to back")},
         "roofline": {"kernel": "tv_tree_attention", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": recorded_traffic(args.workload, args.batch, args.window_left),
                      "peak_source": peak_kind},
-        "e2e": {"value": job_throughput(world, 1, e2e_ms), "unit": "steps/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "h2d_gbs": h2d * e2e_value / 1e9,
+                "h2d_link": link,
+                "frac_of_link": (h2d * e2e_value / 1e9) / link_peak if link_peak else None},
         "gpu_launches": launches_per_step * K,
         "status_ok": status_ok,
-        "clocks": clocks,
+        "clocks": sampler.summary(t_run0, t_run1, "whole measurement: warm-up, timed loop, "
+                                  "sustained loop, attention and end-to-end timing"),
+        "clocks_timed_loop": sampler.summary(t_loop0, t_loop1, "timed loop"),
+        "sustained": {"ms_per_step": sus_ms, "steps_per_s": 1000.0 / sus_ms, "steps": n_sus,
+                      "seconds": round(t_sus1 - t_sus0, 3),
+                      "clocks": sampler.summary(t_sus0, t_sus1, "sustained loop")},
     }
-    if world == 1:
+    if world == 1 and not args.quick:
         # the same step with tv_argmax on 16 SMs beside the attention (two streams)
         line["overlapped_step"] = measure_overlap(args.workload, inp, min(K, 300), dev)
         # the draft-tree path (the step before verify), timed on its own
@@ -893,8 +1092,14 @@ def bench_reference(args, rank, world):
         "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1000.0 / value, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": workload_config(args.workload, args.batch),
+        "config": workload_config(args.workload, args.batch,
+                                  l2="not applicable: the oracle runs on the host cores"),
         "cpu_baseline": cb,
+        # what ran: one sequence per step (and `heads` of the query heads); the
+        # line's value and ms_per_step are that time scaled to the whole batch
+        "scaled_from": {"sequences_timed_per_step": 1, "batch": Bj, "query_heads_timed": heads,
+                        "query_heads": Hq, "steps_timed": K, "wall_s_timed": elapsed,
+                        "factor": Bj * Hq / heads if heads else None},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": elapsed,
     }
