@@ -66,3 +66,18 @@ def assert_close(got, ref, what=""):
     bad = err > bound
     assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
                            f"max err {err.max():.3e}")
+
+
+def run_attention(tv, inp, num_splits=0, window_left=None, kernel=0):
+    B, N = inp["B"], inp["N"]
+    wl = inp["window_left"] if window_left is None else window_left
+    anc = torch.empty((B, N), dtype=torch.int64, device="cuda")
+    pos = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    st = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(inp["q"])
+    tv.tv_build_ancestors(inp["parent"], inp["depth"], inp["ctx_len"], anc, pos, st)
+    tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], inp["k_cache"], inp["v_cache"],
+                         inp["block_table"], inp["ctx_len"], pos, anc, out, st, window_left=wl,
+                         num_splits=num_splits, kernel=kernel)
+    torch.cuda.synchronize()
+    return out, st

@@ -34,7 +34,8 @@ from ._lib import (  # noqa: F401
     tv_build_tree, tv_commit_kv, tv_topk, tv_topk_workspace_size, tv_tree_attention,
     tv_tree_attention_workspace_size, tv_tree_walk, tv_gdn_commit, tv_gdn_tree_verify,
     tv_verify_graph_create,
-    tv_verify_graph_destroy, tv_verify_graph_launch, tv_verify_graph_launches, tv_verify_step)
+    tv_verify_graph_destroy, tv_verify_graph_launch, tv_verify_graph_launches, tv_verify_step,
+    tv_debug_withhold_arrival)
 from ._lib import step_args as _step_args
 
 

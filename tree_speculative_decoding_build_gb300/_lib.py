@@ -47,6 +47,7 @@ EXPORTS = (
     "tv_verify_graph_destroy",
     "tv_gdn_tree_verify",
     "tv_gdn_commit",
+    "tv_debug_withhold_arrival",
 )
 
 
@@ -132,6 +133,8 @@ def _load():
     lib.tv_verify_graph_destroy.restype = None
     lib.tv_gdn_tree_verify.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, P, P, I, P, P]
     lib.tv_gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
+    lib.tv_debug_withhold_arrival.argtypes = [I]
+    lib.tv_debug_withhold_arrival.restype = None
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
               "tv_commit_kv", "tv_topk", "tv_build_tree", "tv_verify_step",
               "tv_verify_graph_create", "tv_verify_graph_launch", "tv_gdn_tree_verify",
@@ -430,3 +433,10 @@ def tv_gdn_commit(state_in, k, u, alpha, acc_nodes, n_acc, state_out, status=Non
         _ptr(alpha, f32, "alpha"), _ptr(acc_nodes, i32, "acc_nodes"), _ptr(n_acc, i32, "n_acc"),
         B, N, Hk, Hv, dk, dv, _ptr(state_out, f32, "state_out"),
         _ptr(status, i32, "status") if status is not None else None, _stream(stream)))
+
+
+def tv_debug_withhold_arrival(cta):
+    """Test hook (include/tv_debug.h): from the next launch on, the tensor-core
+    kernels' CTA ``cta`` waits for a barrier arrival that never comes, so its
+    bounded wait runs out; a negative ``cta`` disarms it."""
+    lib.tv_debug_withhold_arrival(int(cta))

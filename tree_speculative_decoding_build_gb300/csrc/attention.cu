@@ -529,6 +529,7 @@ extern "C" tv_status tv_tree_attention(const tv_attn_args *a, void *workspace,
   p.status = a->status;
   if (a->max_ctas < 0) return TV_ERR_ARG;
   p.ctas = a->max_ctas;
+  p.withheld_cta = debug_withheld_cta();
   cudaStream_t s = as_stream(stream);
   if (tc) {
     if (launch_attention_tc(p, workspace, s) != cudaSuccess) return TV_ERR_CUDA;

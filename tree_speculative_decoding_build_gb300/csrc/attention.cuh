@@ -29,6 +29,7 @@ struct AttnParams {
   __nv_bfloat16 *out;    // [B, N, Hq, D]
   int32_t *status;       // [B]
   int ctas;              // tensor-core kernel: persistent CTAs (0 = one per SM)
+  int withheld_cta;      // test hook: CTA whose first K/V barrier expects an extra arrival (-1: none)
 };
 
 // First visible context block of a sequence: rows sit at positions

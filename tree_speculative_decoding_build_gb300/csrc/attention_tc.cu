@@ -323,7 +323,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
   }
   if (tid == 32 * 2) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars.kv_full[s]), 1);
+      // test hook: one arrival more than the producer makes, in one CTA
+      mbar_init(smem_u32(&bars.kv_full[s]), (s == 0 && (int)blockIdx.x == p.withheld_cta) ? 2 : 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.q_full), 128);

@@ -149,7 +149,9 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   }
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars.kv_full[s]), 1);
+      // test hook: one arrival more than the producer makes, in one CTA
+      const bool held = s == 0 && (int)(blockIdx.y * gridDim.x + blockIdx.x) == p.withheld_cta;
+      mbar_init(smem_u32(&bars.kv_full[s]), held ? 2 : 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
     }
     mbar_init(smem_u32(&bars.q_full), 128);

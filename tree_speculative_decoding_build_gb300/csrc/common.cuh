@@ -31,4 +31,9 @@ inline cudaStream_t as_stream(tv_stream s) { return reinterpret_cast<cudaStream_
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Test hook (tv_debug.h): the CTA, by linear index, whose first-copy barrier
+// the tensor-core kernels set to expect one arrival more than it gets; -1
+// (the default) for none.  Host state, read at every launch.
+int debug_withheld_cta();
+
 }  // namespace tv

@@ -738,7 +738,8 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
                             const float *__restrict__ alpha, const float *__restrict__ beta,
                             const uint64_t *__restrict__ anc, int B, int N, int Hk, int Hv,
                             int dk, int dv, float *__restrict__ out, float *__restrict__ u_out,
-                            float *__restrict__ g_out, int32_t *__restrict__ status) {
+                            float *__restrict__ g_out, int32_t *__restrict__ status,
+                            int withheld_cta) {
   extern __shared__ unsigned char smem_raw[];
   __shared__ PipeBars bars;
   __shared__ uint32_t s_tmem;
@@ -760,7 +761,8 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
   }
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_u32(&bars.s0_full[i]), 1);
+      // test hook: one arrival more than the state copy makes, in one CTA
+      ptx::mbar_init(ptx::smem_u32(&bars.s0_full[i]), (i == 0 && (int)blockIdx.x == withheld_cta) ? 2 : 1);
       ptx::mbar_init(ptx::smem_u32(&bars.kqv_full[i]), 33);
       s_s0cnt[i] = 0;
       ptx::mbar_init(ptx::smem_u32(&bars.d_full[i]), 1);
@@ -1237,7 +1239,8 @@ tv_status launch_gdn_pipe(const float *state, const __nv_bfloat16 *q, const __nv
   const int items = B * Hv;
   const int grid = items < sm_count() ? items : sm_count();
   gdn_tree_verify_pipe_kernel<<<grid, kPipeThreads, kPipeSmem, stream>>>(
-      ms, mk, mq, mv, alpha, beta, anc, B, N, Hk, Hv, dk, dv, out, u, g, status);
+      ms, mk, mq, mv, alpha, beta, anc, B, N, Hk, Hv, dk, dv, out, u, g, status,
+      debug_withheld_cta());
   return launch_status();
 }
 

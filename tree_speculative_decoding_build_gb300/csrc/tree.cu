@@ -13,9 +13,18 @@
 #include <mutex>
 #include <vector>
 
+#include <atomic>
+
 #include "common.cuh"
+#include "tv_debug.h"
 
 namespace tv {
+
+namespace {
+std::atomic<int> g_withheld_cta{-1};
+}  // namespace
+
+int debug_withheld_cta() { return g_withheld_cta.load(std::memory_order_relaxed); }
 
 int sm_count() {
   static std::mutex mu;
@@ -244,4 +253,8 @@ extern "C" tv_status tv_commit_kv(const void *k_tree, const void *v_tree, const 
       ctx_len_in, block_table, N, Hkv, D, max_blocks, num_blocks, static_cast<uint4 *>(k_cache),
       static_cast<uint4 *>(v_cache), ctx_len_out, status);
   return launch_status();
+}
+
+extern "C" void tv_debug_withhold_arrival(int cta) {
+  tv::g_withheld_cta.store(cta < 0 ? -1 : cta, std::memory_order_relaxed);
 }
