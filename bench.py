@@ -496,7 +496,7 @@ def bench_ours(args, rank, world, local):
     status_ok = bool((step.out.status == 0).all().item())
 
     # sustained: the same replays for at least a second, with their own clock record
-    n_sus = max(1, int(math.ceil(1000.0 / max(ms / K, 1e-3))))
+    n_sus = max(1, int(math.ceil(1250.0 / max(ms / K, 1e-3))))
     t_sus0 = time.time()
     s0 = torch.cuda.Event(enable_timing=True)
     s1 = torch.cuda.Event(enable_timing=True)
