@@ -35,7 +35,7 @@ from ._lib import (  # noqa: F401
     tv_tree_attention_workspace_size, tv_tree_walk, tv_gdn_commit, tv_gdn_tree_verify,
     tv_verify_graph_create,
     tv_verify_graph_destroy, tv_verify_graph_launch, tv_verify_graph_launches, tv_verify_step,
-    tv_debug_withhold_arrival)
+    tv_debug_withhold_arrival, tv_debug_check_failures, tv_debug_checks_enabled)
 from ._lib import step_args as _step_args
 
 

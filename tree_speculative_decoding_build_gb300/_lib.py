@@ -17,7 +17,9 @@ import torch
 from . import build as _build
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = _build.LIB
+# TV_LIB_PATH selects another build of the same library (the TV_DEBUG build's
+# libtv_debug.so); by default the release build
+LIB_PATH = os.environ.get("TV_LIB_PATH") or _build.LIB
 
 (TV_OK, TV_ERR_ARG, TV_ERR_TREE, TV_ERR_BLOCK, TV_ERR_CUDA, TV_ERR_UNSUPPORTED,
  TV_ERR_SCRATCH_LIMIT) = range(7)
@@ -48,6 +50,8 @@ EXPORTS = (
     "tv_gdn_tree_verify",
     "tv_gdn_commit",
     "tv_debug_withhold_arrival",
+    "tv_debug_checks_enabled",
+    "tv_debug_check_failures",
 )
 
 
@@ -135,6 +139,10 @@ def _load():
     lib.tv_gdn_commit.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P, P]
     lib.tv_debug_withhold_arrival.argtypes = [I]
     lib.tv_debug_withhold_arrival.restype = None
+    lib.tv_debug_checks_enabled.argtypes = []
+    lib.tv_debug_checks_enabled.restype = I
+    lib.tv_debug_check_failures.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(I), I]
+    lib.tv_debug_check_failures.restype = ctypes.c_uint
     for f in ("tv_build_ancestors", "tv_tree_attention", "tv_argmax", "tv_tree_walk",
               "tv_commit_kv", "tv_topk", "tv_build_tree", "tv_verify_step",
               "tv_verify_graph_create", "tv_verify_graph_launch", "tv_gdn_tree_verify",
@@ -440,3 +448,23 @@ def tv_debug_withhold_arrival(cta):
     kernels' CTA ``cta`` waits for a barrier arrival that never comes, so its
     bounded wait runs out; a negative ``cta`` disarms it."""
     lib.tv_debug_withhold_arrival(int(cta))
+
+
+DEBUG_RECORDS = ("tree.cu", "argmax.cu", "attention.cu", "attention_tc.cu", "attention_tc256.cu",
+                 "draft.cu", "gdn.cu")
+
+
+def tv_debug_check_failures(clear=False):
+    """Index checks of the TV_DEBUG build that failed since the last clear:
+    (count, first failing source file or None, its line).  Always (0, None, 0)
+    for the release build (tv_debug_checks_enabled() == 0)."""
+    line = ctypes.c_uint(0)
+    which = ctypes.c_int(-1)
+    n = int(lib.tv_debug_check_failures(ctypes.byref(line), ctypes.byref(which), int(bool(clear))))
+    if n == 0xFFFFFFFF:
+        raise TvError("tv_debug_check_failures", TV_ERR_CUDA)
+    return n, (DEBUG_RECORDS[which.value] if which.value >= 0 else None), int(line.value)
+
+
+def tv_debug_checks_enabled():
+    return bool(lib.tv_debug_checks_enabled())

@@ -18,6 +18,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtv.so")
+# the TV_DEBUG build (index checks in every kernel, see common.cuh) lives apart
+DEBUG_BUILD = os.path.join(HERE, "_build_debug")
+DEBUG_LIB = os.path.join(DEBUG_BUILD, "libtv_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]
@@ -42,23 +45,30 @@ def _deps():
             glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libtv.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(os.path.join(BUILD, "obj"), exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link libtv.so; returns its path.  ``debug`` (or -DTV_DEBUG
+    among ``extra_flags``) builds the index-checked library libtv_debug.so in
+    its own folder instead."""
+    extra_flags = list(extra_flags)
+    debug = debug or "-DTV_DEBUG" in extra_flags
+    if debug and "-DTV_DEBUG" not in extra_flags:
+        extra_flags.append("-DTV_DEBUG")
+    build_dir, lib = (DEBUG_BUILD, DEBUG_LIB) if debug else (BUILD, LIB)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(os.path.join(build_dir, "obj"), exist_ok=True)
     cc = nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, "obj", os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, "obj", os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -69,13 +79,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

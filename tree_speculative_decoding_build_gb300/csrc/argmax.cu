@@ -35,6 +35,8 @@
 
 #include "common.cuh"
 
+TV_DEBUG_RECORD(argmax)
+
 namespace tv {
 
 namespace {
@@ -151,7 +153,8 @@ argmax_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int ch
   best = block_reduce(best);
   if (threadIdx.x == 0) {
     if (best.i == INT32_MAX) best.i = begin;  // empty chunk cannot happen; keep in range
-    if (chunks == 1) {
+    if (!TV_CHECK(best.i >= begin && best.i < end)) {
+    } else if (chunks == 1) {
       out_idx[row] = best.i;
     } else {
       part_v[blockIdx.x] = best.v;
@@ -261,7 +264,8 @@ argmax_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long 
     if (lane == 0) {
       const long long ps = max(rs, v0);
       const int idx = b.i == INT32_MAX ? (int)((ps - rs) * E) : b.i;
-      if (ps == rs && pe == rs + vpr) {
+      if (!TV_CHECK(idx >= 0 && idx < vpr * E && r < nv / vpr && 2 * w + 1 < 2 * owners)) {
+      } else if (ps == rs && pe == rs + vpr) {
         out_idx[r] = idx;
       } else {
         const long long slot = 2 * w + (ps == v0 ? 0 : 1);
@@ -341,10 +345,11 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
     const long long s0 = str_split(c, nv, owners);
     if (s0 == str_split(c + 1, nv, owners)) continue;  // empty range
     const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
+    if (!TV_CHECK(c < owners)) continue;
     merge(me, Best{part_v[slot], part_i[slot]});
   }
   me = warp_best(me);
-  if (lane == 0) out_idx[r] = me.i;
+  if (lane == 0 && TV_CHECK(r < nv / vpr && me.i >= 0 && me.i < vpr * (16 / 2))) out_idx[r] = me.i;
 }
 
 // ------------------------------------------------------------------ planning

@@ -20,6 +20,8 @@
 
 #include "attention.cuh"
 
+TV_DEBUG_RECORD(attention)
+
 namespace tv {
 
 namespace {
@@ -86,6 +88,7 @@ attn_generic_kernel(const AttnParams p) {
   for (int i = tid; i < nrows * (D / 4); i += kCcThreads) {
     const int rr = i / (D / 4), c4 = i - rr * (D / 4);
     const int r = r0 + rr, t = r / p.G, g = r - t * p.G;
+    if (!TV_CHECK(b < p.B && t < p.N && kvh * p.G + g < p.Hq)) continue;
     const __nv_bfloat16 *src = p.q + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * D + c4 * 4;
     const uint2 w = *reinterpret_cast<const uint2 *>(src);
     float4 f = make_float4(bf16_lo(w.x) * p.qscale, bf16_hi(w.x) * p.qscale,
@@ -94,6 +97,7 @@ attn_generic_kernel(const AttnParams p) {
   }
   for (int rr = tid; rr < nrows; rr += kCcThreads) {
     const int t = (r0 + rr) / p.G;
+    if (!TV_CHECK(t < p.N && rr < kCcRows)) continue;
     s_rpos[rr] = p.pos[(size_t)b * p.N + t];
     s_ranc[rr] = p.anc[(size_t)b * p.N + t];
   }
@@ -107,7 +111,8 @@ attn_generic_kernel(const AttnParams p) {
     constexpr int W = D / 8;  // 16-byte words per row
     if (i < n_ctx_tiles) {
       const int slot = t_begin + i;
-      const int blk = p.block_table[(size_t)b * p.max_blocks + slot];
+      const int blk = TV_CHECK(slot >= 0 && slot < p.max_blocks)
+                          ? p.block_table[(size_t)b * p.max_blocks + slot] : -1;
       const bool blk_ok = blk >= 0 && blk < p.num_blocks;
       if (tid == 0) {
         s_tile_ok[st] = blk_ok;
@@ -257,6 +262,7 @@ attn_generic_kernel(const AttnParams p) {
     const int r = r0 + rr;
     if (p.splits == 1) {
       const int t = r / p.G, g = r - t * p.G;
+      if (!TV_CHECK(t < p.N && kvh * p.G + g < p.Hq)) continue;
       const float inv = l[j] > 0.f ? 1.f / l[j] : 0.f;
       __nv_bfloat16 *dst = p.out + (((size_t)b * p.N + t) * p.Hq + kvh * p.G + g) * D + lane * DL;
 #pragma unroll
@@ -265,6 +271,7 @@ attn_generic_kernel(const AttnParams p) {
             __floats2bfloat162_rn(o[j][e] * inv, o[j][e + 1] * inv);
     } else {
       const size_t row = ((size_t)bk * p.splits + split) * p.R + r;
+      if (!TV_CHECK(row < (size_t)p.B * p.Hkv * p.splits * p.R)) continue;
       float *dst = p.part_o + row * D + lane * DL;
 #pragma unroll
       for (int e = 0; e < DL; ++e) dst[e] = o[j][e];

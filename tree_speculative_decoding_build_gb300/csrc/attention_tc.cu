@@ -60,6 +60,8 @@
 #include "attention.cuh"
 #include "tc_ptx.cuh"
 
+TV_DEBUG_RECORD(attention_tc)
+
 namespace tv {
 namespace {
 
@@ -376,7 +378,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
     int win_base = 0, cur_id = -1, nxt_id = -1;
     bool ok = true;
     auto load_id = [&](int b, int slot) -> int {
-      return slot < nblk_end ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
+      return (slot < nblk_end && TV_CHECK(b < B && slot >= 0 && slot < p.max_blocks))
+                 ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
     };
     while (ok && cur.valid()) {
       const int b = cur.b, kvh = cur.kvh;
@@ -711,9 +714,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           uint32_t qr[2][32];
           const uint4 *src = reinterpret_cast<const uint4 *>(
               p.q + (((size_t)b * N + t) * p.Hq + kvh * G + g) * kD);
+          const bool q_ok = row_ok && TV_CHECK(b < B && t < N && kvh * G + g < p.Hq);
 #pragma unroll
           for (int v = 0; v < 16; ++v) {
-            const uint4 w = row_ok ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+            const uint4 w = q_ok ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
             qr[v >> 3][(v & 7) * 4 + 0] = w.x;
             qr[v >> 3][(v & 7) * 4 + 1] = w.y;
             qr[v >> 3][(v & 7) * 4 + 2] = w.z;
@@ -727,7 +731,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
         }
         q_next_loaded = false;
         allowed = 0;
-        if (row_ok) {
+        if (row_ok && TV_CHECK(b < B && t < N)) {
           pos_t = p.pos[(size_t)b * N + t];
           allowed = p.anc[(size_t)b * N + t];
           if (wl >= 0) {
@@ -912,7 +916,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
           const int slot = 2 * (int)blockIdx.x + (seg_f0 == lo ? 0 : 1);
           float *dst = tp.part_o + (size_t)slot * kD * kM + m;  // dim-major: dim d at d * 128
 #pragma unroll 1
-          for (int c = c_lo; c < c_hi; ++c) {
+          for (int c = c_lo; c < c_hi && TV_CHECK(slot < 2 * (int)gridDim.x); ++c) {
             uint32_t o0[32], o1[32];
             tmem_ld32(t_o0 + c * 32, o0);
             tmem_ld32(t_o1 + c * 32, o1);
@@ -922,7 +926,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
               dst[(size_t)(c * 32 + e) * kM] = (w0 > 0.f ? __uint_as_float(o0[e]) * w0 : 0.f) +
                                                (w1 > 0.f ? __uint_as_float(o1[e]) * w1 : 0.f);
           }
-          if (x == 0) tp.part_ml[(size_t)slot * kM + m] = make_float2(M, L);
+          if (x == 0 && TV_CHECK(slot < 2 * (int)gridDim.x)) tp.part_ml[(size_t)slot * kM + m] = make_float2(M, L);
           if (seg_f0 == cur.f - cur.u) {  // the piece holds the pair's first tile
             own_s = seg_f0;
             own_e = seg_f0 + cur.tiles;
@@ -1007,6 +1011,7 @@ __global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp,
       }
       if (ld == hd) continue;  // an empty range holds no piece
       const int slot = 2 * d + ((d == c && ld < S) ? 1 : 0);
+      if (!TV_CHECK(slot < 2 * P && d0 + 32 <= kD)) continue;
       const float2 ml = __ldcg(tp.part_ml + (size_t)slot * kM + m);
       const float *src = tp.part_o + ((size_t)slot * kD + d0) * kM + m;
       float o[32];

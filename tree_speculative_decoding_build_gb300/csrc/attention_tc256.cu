@@ -38,6 +38,8 @@
 #include "attention.cuh"
 #include "tc_ptx.cuh"
 
+TV_DEBUG_RECORD(attention_tc256)
+
 namespace tv {
 namespace {
 
@@ -197,7 +199,8 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           const int slot = slot0 + i;
           int r = slot < rg.t_stop ? ctx - slot * kBlock : 0;
           r = r < 0 ? 0 : (r > kBlock ? kBlock : r);
-          int id = r > 0 ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
+          int id = (r > 0 && TV_CHECK(b < p.B && slot >= 0 && slot < p.max_blocks))
+                       ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
           if (r > 0 && (id < 0 || id >= p.num_blocks)) {
             if (lane == 0) set_status(p.status, b, TV_ERR_BLOCK);
             r = 0;
@@ -347,7 +350,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int wl = p.window_left;
     int pos_t = 0;
     unsigned long long allowed = 0;
-    if (row_ok) {
+    if (row_ok && TV_CHECK(b < p.B && t < N)) {
       pos_t = p.pos[(size_t)b * N + t];
       allowed = p.anc[(size_t)b * N + t];
       if (wl >= 0) {
@@ -367,7 +370,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         uint32_t qr[32];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 w = row_ok ? __ldg(src + 8 * c + v) : make_uint4(0, 0, 0, 0);
+          const uint4 w = (row_ok && TV_CHECK(kvh * G + g < p.Hq)) ? __ldg(src + 8 * c + v) : make_uint4(0, 0, 0, 0);
           qr[4 * v] = w.x;
           qr[4 * v + 1] = w.y;
           qr[4 * v + 2] = w.z;
@@ -496,6 +499,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         }
       } else {
         const size_t row = ((size_t)bk * p.splits + split) * R + m;
+        const bool row_in = row_ok && TV_CHECK(row < (size_t)p.B * p.Hkv * p.splits * R);
         if (rg.n_tiles > 0) {
           float *dst = p.part_o + row * kD;
 #pragma unroll 1
@@ -503,7 +507,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             uint32_t o[32];
             tmem_ld32(tlane + kColO + c * 32, o);
             tmem_wait_ld();
-            if (row_ok) {
+            if (row_in) {
 #pragma unroll
               for (int e = 0; e < 32; e += 4)
                 *reinterpret_cast<float4 *>(dst + c * 32 + e) =
@@ -512,7 +516,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             }
           }
         }
-        if (row_ok) p.part_ml[row] = make_float2(rg.n_tiles > 0 ? m_used : -INFINITY, l);
+        if (row_in) p.part_ml[row] = make_float2(rg.n_tiles > 0 ? m_used : -INFINITY, l);
       }
     }
     if (!ok && lane == 0) set_status(p.status, b, TV_ERR_CUDA);

@@ -20,6 +20,45 @@ __device__ __forceinline__ void set_status(int32_t *status, int b, int code) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Index checks of the TV_DEBUG build (a stand-in for a memory checker).
+// TV_CHECK(cond) guards one access: in a build with -DTV_DEBUG a false
+// condition is recorded in this translation unit's fault record (the number
+// of failed checks and the source line of the first) and the access is
+// skipped; without TV_DEBUG it is the constant true and the compiled code is
+// that of the plain build.  Each .cu file that uses it names its record once
+// with TV_DEBUG_RECORD(name); tv_debug_check_failures() (tv_debug.h) reads
+// them all.
+#ifdef TV_DEBUG
+#define TV_DEBUG_RECORD(name)                                                   \
+  namespace tv {                                                                \
+  static __device__ unsigned int g_check_record[2];                             \
+  static __device__ __noinline__ bool check_failed(int line) {                  \
+    if (atomicAdd(&g_check_record[0], 1u) == 0u) g_check_record[1] = (unsigned)line; \
+    return false;                                                               \
+  }                                                                             \
+  unsigned debug_record_##name(unsigned *first_line, bool clear) {              \
+    unsigned r[2] = {0u, 0u};                                                   \
+    if (cudaMemcpyFromSymbol(r, g_check_record, sizeof(r)) != cudaSuccess) return ~0u; \
+    if (clear) {                                                                \
+      const unsigned z[2] = {0u, 0u};                                           \
+      cudaMemcpyToSymbol(g_check_record, z, sizeof(z));                         \
+    }                                                                           \
+    if (first_line) *first_line = r[1];                                         \
+    return r[0];                                                                \
+  }                                                                             \
+  }
+#define TV_CHECK(cond) ((cond) || tv::check_failed(__LINE__))
+#else
+#define TV_DEBUG_RECORD(name)                                                   \
+  namespace tv {                                                                \
+  unsigned debug_record_##name(unsigned *first_line, bool) {                    \
+    if (first_line) *first_line = 0u;                                           \
+    return 0u;                                                                  \
+  }                                                                             \
+  }
+#define TV_CHECK(cond) true
+#endif
+
 // Host side: translate the last CUDA error into a status code.
 inline tv_status launch_status() {
   cudaError_t e = cudaGetLastError();

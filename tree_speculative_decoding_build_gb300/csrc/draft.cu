@@ -41,6 +41,8 @@
 #include "common.cuh"
 #include "tv_draft.h"
 
+TV_DEBUG_RECORD(draft)
+
 namespace tv {
 
 namespace {
@@ -341,7 +343,7 @@ topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chun
     }
   }
   block_fold(lv, li, k);
-  if (w == 0 && lane < k) {
+  if (w == 0 && lane < k && TV_CHECK(li == INT32_MAX || (li >= 0 && li < V))) {
     out_v[(size_t)blockIdx.x * k + lane] = lv;
     out_i[(size_t)blockIdx.x * k + lane] = li;
   }
@@ -805,7 +807,7 @@ build_tree_kernel(const float *cand_lp, const int32_t *cand_idx, int B, int L, i
       if (lane == src) {
 #pragma unroll
         for (int u = 0; u < kBtSlots; ++u) {  // static indices keep the cursors in registers
-          if (u == bu) {
+          if (u == bu && TV_CHECK(n < budget && n < TV_MAX_NODES && dep[u] >= 1 && dep[u] <= L && nr[u] >= 0 && nr[u] < K)) {
             psc = sc[u];
             pdep = dep[u];
             s.node_score[n] = sc[u];

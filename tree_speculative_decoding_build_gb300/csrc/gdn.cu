@@ -34,6 +34,8 @@
 #include "tc_ptx.cuh"
 #include "tv_gdn.h"
 
+TV_DEBUG_RECORD(gdn)
+
 namespace tv {
 namespace {
 
@@ -278,12 +280,13 @@ gdn_tree_verify_kernel(const float *__restrict__ state, const __nv_bfloat16 *__r
     const int t = w + kGdnWarps * r;
     if (t < N) {
       float o0 = sg[t] * accr[r][0], o1 = sg[t] * accr[r][1];
-      for (int i = t; i >= 0; i = spar[i]) {
+      for (int i = t; i >= 0; i = TV_CHECK(spar[i] < i) ? spar[i] : -1) {
         const float y = sY[t * (N + 1) + i];
         o0 = fmaf(y, sU[i * kGdnUStride + lane], o0);
         o1 = fmaf(y, sU[i * kGdnUStride + lane + 32], o1);
       }
       const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + j0;
+      if (!TV_CHECK(dst + 32 < (size_t)gridDim.z * N * Hv * dv)) continue;
       out[dst] = o0;
       out[dst + 32] = o1;
       u_out[dst] = sU[t * kGdnUStride + lane];
@@ -605,12 +608,13 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
   for (int t = w; t < N; t += kGdnWarps) {
     const float gt = sg[t];
     float o0 = gt * sR[t * kGdnUStride + lane], o1 = gt * sR[t * kGdnUStride + lane + 32];
-    for (int i = t; i >= 0; i = spar[i]) {
+    for (int i = t; i >= 0; i = TV_CHECK(spar[i] < i) ? spar[i] : -1) {
       const float y = sY[t * (N + 1) + i];
       o0 = fmaf(y, sU[i * kGdnUStride + lane], o0);
       o1 = fmaf(y, sU[i * kGdnUStride + lane + 32], o1);
     }
     const size_t dst = (((size_t)b * N + t) * Hv + h) * dv + (size_t)c * kTcCols + lane;
+    if (!TV_CHECK(dst + 32 < (size_t)gridDim.z * N * Hv * dv)) continue;
     out[dst] = o0;
     out[dst + 32] = o1;
     u_out[dst] = sU[t * kGdnUStride + lane];
@@ -1016,7 +1020,7 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
       //    the outputs (Q S_0)
       const size_t o0 = ((size_t)b * N * Hv + h) * dv + j, rs = (size_t)Hv * dv;
       float *uo = u_out + o0, *oo = out + o0;
-      const bool mine = j < dv;
+      const bool mine = j < dv && TV_CHECK(b < B && h < Hv);
       // U and the products run on pairs (packed fp32 FMA, one rounding per
       // element as fmaf): U2[p] = (u_2p, u_2p+1), rows of X and Y in pairs of
       // columns.  X and Y are zero past each row's own column, and U starts at
@@ -1145,6 +1149,7 @@ gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__res
   const float gl = s_gl;
   for (int e = threadIdx.x; e < L * dk; e += kGcThreads) {
     const int p = e / dk, i = e - p * dk;
+    if (!TV_CHECK(spath[p] >= 0 && spath[p] < N)) continue;
     sku[e] = __bfloat162float(k[(((size_t)b * N + spath[p]) * Hk + hk) * dk + i]);
   }
   for (int e = threadIdx.x; e < L * kGcDC; e += kGcThreads) {

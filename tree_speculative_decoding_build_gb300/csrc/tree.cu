@@ -18,6 +18,8 @@
 #include "common.cuh"
 #include "tv_debug.h"
 
+TV_DEBUG_RECORD(tree)
+
 namespace tv {
 
 namespace {
@@ -75,8 +77,10 @@ __global__ void build_ancestors_kernel(const int32_t *__restrict__ parent,
       bad = true;
       m = 1ull << t;
     }
-    anc[(size_t)b * N + t] = m;
-    pos[(size_t)b * N + t] = ctx - 1 + dep[t];
+    if (TV_CHECK(t >= 0 && t < N)) {
+      anc[(size_t)b * N + t] = m;
+      pos[(size_t)b * N + t] = ctx - 1 + dep[t];
+    }
   }
   bad = __any_sync(0xffffffffu, bad);
   if (lane == 0) status[b] = bad ? TV_ERR_TREE : TV_OK;
@@ -112,6 +116,7 @@ __global__ void tree_walk_kernel(const int32_t *__restrict__ tokens,
       const unsigned m1 = __ballot_sync(0xffffffffu, t1 < N && par1 == cur && tok1 == pred);
       const int c = m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : -1);
       if (c < 0) break;
+      if (!TV_CHECK(c < N && k < N)) break;
       if (lane == 0) path[w][k] = c;
       ++k;
       cur = c;
@@ -123,7 +128,7 @@ __global__ void tree_walk_kernel(const int32_t *__restrict__ tokens,
   int32_t *an = acc_nodes + base;
   for (int i = lane; i <= N; i += 32) {
     int v = -1;
-    if (i < k) v = tokens[base + path[w][i]];
+    if (i < k && TV_CHECK(path[w][i] >= 0 && path[w][i] < N)) v = tokens[base + path[w][i]];
     else if (i == k) v = pred;
     ot[i] = v;
     if (i < N) an[i] = i < k ? path[w][i] : -1;
@@ -181,6 +186,9 @@ __global__ void commit_kv_kernel(const uint4 *__restrict__ k_tree, const uint4 *
     const int p = ctx + r;
     const size_t src = (((size_t)b * N + s_node[r]) * Hkv + h) * words + wd;
     const size_t dst = (((size_t)s_blk[r] * Hkv + h) * kBlock + (p % kBlock)) * words + wd;
+    if (!TV_CHECK(src < (size_t)gridDim.x * N * Hkv * words &&
+                  dst < (size_t)num_blocks * Hkv * kBlock * words && p >= 0))
+      continue;
     k_cache[dst] = k_tree[src];
     v_cache[dst] = v_tree[src];
   }
@@ -257,4 +265,43 @@ extern "C" tv_status tv_commit_kv(const void *k_tree, const void *v_tree, const 
 
 extern "C" void tv_debug_withhold_arrival(int cta) {
   tv::g_withheld_cta.store(cta < 0 ? -1 : cta, std::memory_order_relaxed);
+}
+
+namespace tv {
+unsigned debug_record_argmax(unsigned *, bool);
+unsigned debug_record_attention(unsigned *, bool);
+unsigned debug_record_attention_tc(unsigned *, bool);
+unsigned debug_record_attention_tc256(unsigned *, bool);
+unsigned debug_record_draft(unsigned *, bool);
+unsigned debug_record_gdn(unsigned *, bool);
+}  // namespace tv
+
+extern "C" int tv_debug_checks_enabled(void) {
+#ifdef TV_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+extern "C" unsigned tv_debug_check_failures(unsigned *first_line, int *first_file, int clear) {
+  unsigned (*const rec[])(unsigned *, bool) = {
+      tv::debug_record_tree, tv::debug_record_argmax, tv::debug_record_attention,
+      tv::debug_record_attention_tc, tv::debug_record_attention_tc256, tv::debug_record_draft,
+      tv::debug_record_gdn};
+  unsigned total = 0, line = 0;
+  int file = -1;
+  for (int i = 0; i < (int)(sizeof(rec) / sizeof(rec[0])); ++i) {
+    unsigned l = 0;
+    const unsigned n = rec[i](&l, clear != 0);
+    if (n == ~0u) return ~0u;
+    if (n > 0 && file < 0) {
+      file = i;
+      line = l;
+    }
+    total += n;
+  }
+  if (first_line) *first_line = line;
+  if (first_file) *first_file = file;
+  return total;
 }
