@@ -599,6 +599,7 @@ def bench_ours(args, rank, world, local):
         # the draft-tree path (the step before verify), timed on its own
         d = measure_draft("tree_build", 50, 3, dev)
         d.pop("_inputs")
+        d["top_w"] = measure_top_w(dev)
         line["draft_path"] = d
         # the multi-layer step as one CUDA-graph replay, on the small best-first batch
         line["graph_path"] = measure_graph("best_first", 8, 50, 3, dev)
@@ -720,6 +721,33 @@ def measure_draft(name, steps, warmup, dev, seed_offset=0, batch=None):
     }
 
 
+def measure_top_w(dev, iters=200):
+    """The leaf-sibling proposer's top-W emission on its own shape (4 spine
+    positions x 262144-token vocabulary, W = 4, fp32 log-probabilities):
+    tv_topk alone, timed by CUDA-graph replays, each after an L2 flush (cold)
+    and back to back (its 4 MB stay in L2)."""
+    import torch
+    import workloads
+    import tree_speculative_decoding_build_gb300 as tv
+    w = workloads.DRAFT_WORKLOADS["top_w"]
+    lp = workloads.make_draft("top_w", dev, B=w.B).view(w.B * w.L, w.V)
+    vals = torch.empty(w.B * w.L, w.K, dtype=torch.float32, device=dev)
+    idx = torch.empty(w.B * w.L, w.K, dtype=torch.int32, device=dev)
+    need = tv.tv_topk_workspace_size(w.B * w.L, w.V, w.K, tv.TV_F32)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    fn = lambda: tv.tv_topk(lp, w.K, vals, idx, ws)
+    cold = graph_device_ms(fn, dev, iters, flush=L2Flush(dev))
+    warm = graph_device_ms(fn, dev, max(5, iters // 10), reps=10)
+    nbytes = lp.numel() * lp.element_size() + vals.numel() * 8
+    peak, peak_kind = peaks()
+    return {"workload": f"top_w: {w.B * w.L} rows x V={w.V} fp32 log-probs, W={w.K}",
+            "us": cold * 1000.0, "warm_us": warm * 1000.0, "bytes": nbytes,
+            "gbs": nbytes / (cold * 1e-3) / 1e9, "frac_of_peak": nbytes / (cold * 1e-3) / 1e9 / peak,
+            "peak_source": peak_kind,
+            "timing": "CUDA-graph replays of one tv_topk call, each after an L2 flush; warm_us: "
+                      "10 calls per replay, back to back"}
+
+
 def draft_cpu_baseline(name, budget_s=10.0):
     """The oracle on a bounded sample of the draft workload: whole sequences
     (top-k of every position, then the construction) until the budget is spent."""
@@ -785,6 +813,7 @@ def bench_draft(args, rank, world, local):
                      "frac": r["tv_topk"]["frac_of_peak"], "traffic": None,
                      "peak_source": r["tv_topk"]["peak_source"]},
         "tv_build_tree_us": r["tv_build_tree"]["us"],
+        "top_w": measure_top_w(dev) if world == 1 else None,
         "e2e": {"value": job_throughput(world, 1, e2e_ms), "unit": "steps/s",
                 "h2d_bytes_per_step": lp_host.numel() * lp_host.element_size(),
                 "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in res_host)},
