@@ -72,7 +72,9 @@ tv_status tv_gdn_tree_verify(const float *state, const void *q, const void *k, c
  * tv_gdn_tree_verify).  g_l / g_p is formed as the product of alpha over the
  * path nodes after p, so no division is made.  n_acc = 0, a node index out of
  * range or a non-zero status copies S_0.  state_out may not alias state_in.
- * Errors: TV_ERR_ARG (NULL pointers, sizes out of range, aliasing).
+ * state_in, state_out, k and u must be 16-byte aligned (the state moves in
+ * bulk copies of whole 32-row tiles, k and u rows in 16-byte pieces).
+ * Errors: TV_ERR_ARG (NULL pointers, sizes out of range, aliasing, alignment).
  */
 tv_status tv_gdn_commit(const float *state_in, const void *k, const float *u, const float *alpha,
                         const int32_t *acc_nodes, const int32_t *n_acc, int B, int N, int Hk,

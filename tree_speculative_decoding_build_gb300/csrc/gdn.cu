@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -1089,101 +1090,252 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
   }
 }
 
-constexpr int kGcThreads = 256;
+// ------------------------------------------------------------------ state commit
+//
+// S_out^T[j][i] = g_l S_0^T[j][i] + sum_p gam_p u_p[j] k_p[i] over the accepted
+// path (gam_p: product of alpha over the path nodes after p; g_l: over the
+// whole path).  An item is (sequence, value head, 32 rows of S^T): a 16 KB
+// tile at d_k = 128, contiguous in the [B, Hv, d_v, d_k] state.
+//
+// Persistent: the (sequence, value head) groups of d_v / 32 tiles each are
+// dealt to the CTAs in turn (group g to CTA g mod P), so that at any moment
+// the CTAs read one contiguous stretch of the state (CTAs reading far-apart
+// ranges of their own ran at a third of the rate), and a group's tiles share
+// its path data.
+//   warp 0    state tiles by bulk copy into a ring of 16 KB stages (as many as
+//             the shared memory left by the path buffers holds, <= 12), as far
+//             ahead as the ring allows;
+//   warps 1-3 each group's path data (warp w every third group, into buffer
+//             w - 1, up to three groups ahead): path length, the alphas of the
+//             path nodes, k rows (bf16, as stored) and u rows (fp32, all d_v
+//             columns), by one round of asynchronous copies (the path itself
+//             is read when the sequence changes); under full memory load such a
+//             round takes microseconds, so one warp alone held the pipeline back;
+//   warps 4-11 per tile: read it, free its stage, then the new rows (thread:
+//             up to four 16-byte pieces of the tile), stored straight to
+//             global memory.
+// Every wait is bounded (2 s); a wait that runs out makes every role stop,
+// copies in flight get a bounded chance to land, and the rows of the tiles not
+// reached are left unwritten.
+constexpr int kCpStagesMax = 12;  // the ring takes what shared memory the path buffers leave
+constexpr int kCpConsumers = 256;
+constexpr int kCpSetupBufs = 3;  // path-data buffers, one per path-data warp
+constexpr int kCpThreads = 32 * (1 + kCpSetupBufs) + kCpConsumers;
+constexpr uint32_t kCpTileMax = kGcDC * 128 * 4;  // d_k <= 128
 
-__host__ __device__ inline size_t gc_k_offset(int N) { return ((size_t)N * 8 + 15) / 16 * 16; }
+struct CpBars {
+  unsigned long long full[kCpStagesMax], empty[kCpStagesMax], setup_full[kCpSetupBufs],
+      setup_empty[kCpSetupBufs];
+};
 
-// S_out^T[j][i] = g_l S_0^T[j][i] + sum_p gam_p u_p[j] k_p[i] over the accepted path.
-__global__ void __launch_bounds__(kGcThreads, 8)
-gdn_commit_kernel(const float *__restrict__ state_in, const __nv_bfloat16 *__restrict__ k,
-                  const float *__restrict__ u, const float *__restrict__ alpha,
-                  const int32_t *__restrict__ acc_nodes, const int32_t *__restrict__ n_acc, int N,
-                  int Hk, int Hv, int dk, int dv, float *__restrict__ state_out,
-                  const int32_t *__restrict__ status) {
+// bytes of one path-data buffer for N nodes: header (L), alphas [N],
+// k rows [N][d_k] bf16, u rows [N][d_v] fp32, each part 16-byte aligned
+__host__ __device__ inline uint32_t cp_setup_bytes(int N, int dk, int dv) {
+  const uint32_t gam = ((uint32_t)N * 4 + 15) / 16 * 16;
+  return 16 + gam + (uint32_t)N * dk * 2 + (uint32_t)N * dv * 4;
+}
+
+// bounded wait by every lane of a warp; false when it ran out or another role
+// gave up
+__device__ __forceinline__ bool cp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  return warp_wait(bar, parity, abort_flag);
+}
+
+__global__ void __launch_bounds__(kCpThreads, 1)
+gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfloat16 *__restrict__ k,
+                       const float *__restrict__ u, const float *__restrict__ alpha,
+                       const int32_t *__restrict__ acc_nodes, const int32_t *__restrict__ n_acc,
+                       const int32_t *__restrict__ status, int B, int N, int Hk, int Hv, int dk,
+                       int dv, float *__restrict__ state_out, int stages) {
   extern __shared__ __align__(16) unsigned char smem[];
-  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int hk = h / (Hv / Hk);
-  __shared__ int s_len;
-  __shared__ float s_gl;
-  int *spath = reinterpret_cast<int *>(smem);                      // [N]
-  float *sgam = reinterpret_cast<float *>(smem + N * 4);           // [N]
-  float *sku = reinterpret_cast<float *>(smem + gc_k_offset(N));   // [N][dk] k rows, 16-aligned
-  float *suu = sku + (size_t)N * dk;                               // [N][32] u columns
-  if (threadIdx.x < 32) {
-    // the accepted path: node indices and their alphas loaded by the lanes
-    // side by side (two per lane, N <= 64), then the products of alpha over
-    // the nodes after each one, in path order from the end (one lane)
-    const int lane = threadIdx.x;
-    int L = (status && status[b] != 0) ? 0 : n_acc[b];
-    if (L < 0 || L > N) L = 0;
-    bool bad = false;
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int p = lane + 32 * h2;
-      if (p < L) {
-        const int t = acc_nodes[(size_t)b * N + p];
-        bad |= t < 0 || t >= N;
-        spath[p] = t;
+  __shared__ CpBars bars;
+  __shared__ int s_abort;
+  __shared__ long long s_issued;  // state tiles the copy warp sent
+  __shared__ int s_path[kCpSetupBufs][kGdnMaxN];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nC = dv / kGcDC;                      // items (tiles) per group
+  const long long groups = (long long)B * Hv;     // (sequence, value head)
+  const uint32_t tile = (uint32_t)kGcDC * dk * 4;
+  const uint32_t sbase = ptx::smem_u32(smem);
+  const uint32_t setup_off = stages * kCpTileMax;
+  const uint32_t setup_bytes = cp_setup_bytes(N, dk, dv);
+  const uint32_t gam_bytes = ((uint32_t)N * 4 + 15) / 16 * 16;
+  if (tid == 0) {
+    for (int i = 0; i < stages; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars.full[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&bars.empty[i]), kCpConsumers);
+    }
+    for (int i = 0; i < kCpSetupBufs; ++i) {
+      ptx::mbar_init(ptx::smem_u32(&bars.setup_full[i]), 32);
+      ptx::mbar_init(ptx::smem_u32(&bars.setup_empty[i]), kCpConsumers);
+    }
+    s_abort = 0;
+    s_issued = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int *abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- state tiles
+    long long n = 0;
+    bool ok = true;
+    for (long long gr = blockIdx.x; ok && gr < groups; gr += gridDim.x) {
+      for (int c = 0; c < nC; ++c, ++n) {
+        const int st = (int)(n % stages);
+        if (n >= stages &&
+            !(ok = cp_wait(ptx::smem_u32(&bars.empty[st]), (uint32_t)(((n / stages) - 1) & 1), abort_flag)))
+          break;
+        if (lane == 0) {
+          // one tensor copy of the tile's 32 rows (256-byte L2 promotion: a
+          // plain bulk copy of the same bytes ran at a third of the rate)
+          const uint32_t fb = ptx::smem_u32(&bars.full[st]);
+          ptx::mbar_arrive_expect_tx(fb, tile);
+          if (n == 0) ptx::prefetch_tensormap(&tm_st);
+          ptx::tma_load_2d(sbase + (uint32_t)st * kCpTileMax, &tm_st, fb, 0, (int)((gr * nC + c) * kGcDC));
+        }
+        __syncwarp();
       }
     }
-    if (__any_sync(0xffffffffu, bad)) L = 0;
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int p = lane + 32 * h2;
-      if (p < L) sgam[p] = alpha[((size_t)b * N + spath[p]) * Hv + h];
-    }
-    __syncwarp();
-    if (lane == 0) {
-      float cur = 1.f;  // product of alpha over the path nodes after p
-      for (int p = L - 1; p >= 0; --p) {
-        const float a = sgam[p];
-        sgam[p] = cur;
-        cur *= a;
+    if (lane == 0) s_issued = n;
+  } else if (warp <= kCpSetupBufs) {
+    // ---------------------------------------------------------- path data
+    // warp w takes the CTA's groups g = w - 1, w - 1 + kCpSetupBufs, ... into
+    // buffer w - 1 (the gathers are latency-bound: several warps keep several
+    // groups' copies in flight).  The path (length, nodes) is read when the
+    // sequence changes; per group one round of asynchronous copies brings the
+    // alphas, k rows and u rows.
+    const int sb = warp - 1;
+    int cur_b = -1, L = 0;
+    int *path = s_path[sb];
+    for (int g = sb; blockIdx.x + (long long)g * gridDim.x < groups; g += kCpSetupBufs) {
+      const long long gr = blockIdx.x + (long long)g * gridDim.x;
+      if (g >= kCpSetupBufs &&
+          !cp_wait(ptx::smem_u32(&bars.setup_empty[sb]), (uint32_t)((g / kCpSetupBufs - 1) & 1), abort_flag))
+        break;
+      const int b = (int)(gr / Hv), h = (int)(gr - (long long)b * Hv), hk = h / (Hv / Hk);
+      if (b != cur_b) {
+        cur_b = b;
+        L = 0;
+        if (lane == 0) {
+          L = (status && status[b] != 0) ? 0 : n_acc[b];
+          if (L < 0 || L > N) L = 0;
+        }
+        const int t0 = lane < N ? acc_nodes[(size_t)b * N + lane] : 0;
+        const int t1 = lane + 32 < N ? acc_nodes[(size_t)b * N + lane + 32] : 0;
+        L = __shfl_sync(0xffffffffu, L, 0);
+        const bool bad = (lane < L && (t0 < 0 || t0 >= N)) || (lane + 32 < L && (t1 < 0 || t1 >= N));
+        if (__any_sync(0xffffffffu, bad)) L = 0;
+        if (lane < L) path[lane] = t0;
+        if (lane + 32 < L) path[lane + 32] = t1;
+        __syncwarp();
       }
-      s_len = L;
-      s_gl = cur;  // g of the last node: the product over the whole path
+      unsigned char *buf = smem + setup_off + (uint32_t)sb * setup_bytes;
+      // alphas of the path nodes (raw: the consumers form the products), k rows, u rows
+      for (int pp = lane; pp < L; pp += 32) {
+        const int t = path[pp];
+        if (TV_CHECK(t >= 0 && t < N))
+          cp_async_zfill(ptx::smem_u32(buf + 16 + pp * 4), alpha + ((size_t)b * N + t) * Hv + h, 4, true);
+      }
+      const int kc = dk / 8, uc = dv / 4;  // 16-byte pieces per k row, per u row
+      for (int e = lane; e < L * kc; e += 32) {
+        const int pp = e / kc, q = e - pp * kc;
+        const int t = path[pp];
+        if (TV_CHECK(t >= 0 && t < N))
+          cp_async16(buf + 16 + gam_bytes + (size_t)pp * dk * 2 + q * 16,
+                     k + (((size_t)b * N + t) * Hk + hk) * dk + q * 8);
+      }
+      for (int e = lane; e < L * uc; e += 32) {
+        const int pp = e / uc, q = e - pp * uc;
+        const int t = path[pp];
+        if (TV_CHECK(t >= 0 && t < N))
+          cp_async16(buf + 16 + gam_bytes + (size_t)N * dk * 2 + (size_t)pp * dv * 4 + q * 16,
+                     u + (((size_t)b * N + t) * Hv + h) * dv + q * 4);
+      }
+      if (lane == 0) reinterpret_cast<int *>(buf)[0] = L;
+      cp_async_wait_all();
+      __syncwarp();
+      ptx::mbar_arrive(ptx::smem_u32(&bars.setup_full[sb]));
+    }
+  } else {
+    // ---------------------------------------------------------- new rows
+    // S_out = g_l S_0 + sum_p gam_p u_p[j] k_p, with gam_p (the product of
+    // alpha over the path nodes after p) formed from the end of the path, and
+    // g_l the product over all of it
+    const int ct = tid - 32 * (1 + kCpSetupBufs);
+    long long n = 0;
+    int g = 0;
+    bool ok = true;
+    constexpr int kIter = kGcDC * 128 / (kCpConsumers * 4);  // 16-byte pieces per thread (<= 4)
+    for (long long gr = blockIdx.x; ok && gr < groups; gr += gridDim.x, ++g) {
+      if (g > 0) ptx::mbar_arrive(ptx::smem_u32(&bars.setup_empty[(g - 1) % kCpSetupBufs]));
+      const int sb = g % kCpSetupBufs;
+      if (!(ok = cp_wait(ptx::smem_u32(&bars.setup_full[sb]), (uint32_t)((g / kCpSetupBufs) & 1), abort_flag)))
+        break;
+      const unsigned char *buf = smem + setup_off + (uint32_t)sb * setup_bytes;
+      const int L = reinterpret_cast<const int *>(buf)[0];
+      const float *al = reinterpret_cast<const float *>(buf + 16);
+      const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(buf + 16 + gam_bytes);
+      const float *us = reinterpret_cast<const float *>(buf + 16 + gam_bytes + (size_t)N * dk * 2);
+      for (int c = 0; c < nC; ++c, ++n) {
+        const int st = (int)(n % stages);
+        if (!(ok = cp_wait(ptx::smem_u32(&bars.full[st]), (uint32_t)((n / stages) & 1), abort_flag))) break;
+        const float *tl = reinterpret_cast<const float *>(smem + (uint32_t)st * kCpTileMax);
+        float4 sv[kIter];
+#pragma unroll
+        for (int i2 = 0; i2 < kIter; ++i2) {
+          const int e = (ct + i2 * kCpConsumers) * 4;
+          if (e < kGcDC * dk) sv[i2] = *reinterpret_cast<const float4 *>(tl + e);
+        }
+        ptx::mbar_arrive(ptx::smem_u32(&bars.empty[st]));  // the stage may be refilled
+        float *dst = state_out + (size_t)(gr * nC + c) * kGcDC * dk;
+        // the path loop outside, the thread's pieces inside: their chains
+        // interleave, and a piece's column of k is one load per node (the
+        // pieces of a thread lie in rows kCpConsumers * 4 / d_k apart, in the
+        // same columns when d_k divides kCpConsumers * 4)
+        float4 acc[kIter];
+        int jj[kIter], ii[kIter];
+#pragma unroll
+        for (int i2 = 0; i2 < kIter; ++i2) {
+          const int e = (ct + i2 * kCpConsumers) * 4;
+          jj[i2] = e / dk;
+          ii[i2] = e - jj[i2] * dk;
+          acc[i2] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float cur = 1.f;
+        for (int pp = L - 1; pp >= 0; --pp) {
+          const float *ur = us + (size_t)pp * dv + c * kGcDC;
+          const __nv_bfloat16 *kr = ks + (size_t)pp * dk;
+#pragma unroll
+          for (int i2 = 0; i2 < kIter; ++i2) {
+            const float up = cur * ur[jj[i2] < kGcDC ? jj[i2] : 0];
+            const uint2 kw = *reinterpret_cast<const uint2 *>(kr + ii[i2]);
+            acc[i2].x = fmaf(up, bf16_lo(kw.x), acc[i2].x);
+            acc[i2].y = fmaf(up, bf16_hi(kw.x), acc[i2].y);
+            acc[i2].z = fmaf(up, bf16_lo(kw.y), acc[i2].z);
+            acc[i2].w = fmaf(up, bf16_hi(kw.y), acc[i2].w);
+          }
+          cur *= al[pp];
+        }
+#pragma unroll
+        for (int i2 = 0; i2 < kIter; ++i2) {
+          const int e = (ct + i2 * kCpConsumers) * 4;
+          if (e >= kGcDC * dk) continue;
+          __stcs(reinterpret_cast<float4 *>(dst + e),  // streamed: written once, not read back here
+                 make_float4(fmaf(sv[i2].x, cur, acc[i2].x), fmaf(sv[i2].y, cur, acc[i2].y),
+                             fmaf(sv[i2].z, cur, acc[i2].z), fmaf(sv[i2].w, cur, acc[i2].w)));
+        }
+      }
     }
   }
   __syncthreads();
-  const int L = s_len;
-  const float gl = s_gl;
-  for (int e = threadIdx.x; e < L * dk; e += kGcThreads) {
-    const int p = e / dk, i = e - p * dk;
-    if (!TV_CHECK(spath[p] >= 0 && spath[p] < N)) continue;
-    sku[e] = __bfloat162float(k[(((size_t)b * N + spath[p]) * Hk + hk) * dk + i]);
-  }
-  for (int e = threadIdx.x; e < L * kGcDC; e += kGcThreads) {
-    const int p = e / kGcDC, jj = e - p * kGcDC;
-    suu[e] = sgam[p] * u[(((size_t)b * N + spath[p]) * Hv + h) * dv + c * kGcDC + jj];
-  }
-  __syncthreads();
-  const size_t base = (((size_t)b * Hv + h) * dv + (size_t)c * kGcDC) * dk;
-  constexpr int kIter = kGcDC * 128 / (kGcThreads * 4);  // at most 4 float4 per thread
-  float4 sv[kIter];
-#pragma unroll
-  for (int it = 0; it < kIter; ++it) {  // every load issued before any is used
-    const int e = (threadIdx.x + it * kGcThreads) * 4;
-    if (e < kGcDC * dk) sv[it] = __ldg(reinterpret_cast<const float4 *>(state_in + base + e));
-  }
-#pragma unroll
-  for (int it = 0; it < kIter; ++it) {
-    const int e = (threadIdx.x + it * kGcThreads) * 4;
-    if (e >= kGcDC * dk) continue;
-    const int jj = e / dk, i = e - jj * dk;
-    float4 s = sv[it];
-    s.x *= gl;
-    s.y *= gl;
-    s.z *= gl;
-    s.w *= gl;
-    for (int p = 0; p < L; ++p) {
-      const float up = suu[p * kGcDC + jj];
-      const float4 k4 = *reinterpret_cast<const float4 *>(sku + (size_t)p * dk + i);
-      s.x = fmaf(up, k4.x, s.x);
-      s.y = fmaf(up, k4.y, s.y);
-      s.z = fmaf(up, k4.z, s.z);
-      s.w = fmaf(up, k4.w, s.w);
-    }
-    *reinterpret_cast<float4 *>(state_out + base + e) = s;
+  if (*abort_flag && tid == 0) {
+    // a role gave up: state copies still in flight get a bounded chance to
+    // land before the CTA leaves
+    int dummy = 0;
+    const long long n = s_issued;
+    for (long long m = n > stages ? n - stages : 0; m < n; ++m)
+      pipe_wait_slow(ptx::smem_u32(&bars.full[m % stages]), (uint32_t)((m / stages) & 1), &dummy);
   }
 }
 
@@ -1312,15 +1464,24 @@ extern "C" tv_status tv_gdn_commit(const float *state_in, const void *k, const f
   if (B == 0) return TV_OK;
   if (!state_in || !k || !u || !alpha || !acc_nodes || !n_acc || !state_out) return TV_ERR_ARG;
   if (state_in == state_out) return TV_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(state_in) | reinterpret_cast<uintptr_t>(state_out)) & 15)
+  if ((reinterpret_cast<uintptr_t>(state_in) | reinterpret_cast<uintptr_t>(state_out) |
+       reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(u)) & 15)
     return TV_ERR_ARG;
-  const size_t smem = gc_k_offset(N) + (size_t)N * dk * 4 + (size_t)N * kGcDC * 4;
-  if (cudaFuncSetAttribute(gdn_commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t setup = kCpSetupBufs * (size_t)cp_setup_bytes(N, dk, dv);
+  const int stages = (int)std::min<size_t>(kCpStagesMax, (220u * 1024u - setup) / kCpTileMax);
+  const size_t smem = (size_t)stages * kCpTileMax + setup;
+  if (cudaFuncSetAttribute(gdn_commit_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return TV_ERR_CUDA;
-  const dim3 grid(dv / kGcDC, Hv, B);
-  gdn_commit_kernel<<<grid, kGcThreads, smem, as_stream(stream)>>>(
-      state_in, static_cast<const __nv_bfloat16 *>(k), u, alpha, acc_nodes, n_acc, N, Hk, Hv, dk,
-      dv, state_out, status);
+  const long long groups = (long long)B * Hv;
+  const int grid = groups < sm_count() ? (int)groups : sm_count();
+  CUtensorMap mst;
+  if (!gdn_map(&mst, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, state_in, (uint64_t)dk,
+               (uint64_t)B * Hv * dv, (uint64_t)dk * 4, (uint32_t)dk, (uint32_t)kGcDC,
+               CU_TENSOR_MAP_SWIZZLE_NONE))
+    return TV_ERR_CUDA;
+  gdn_commit_pipe_kernel<<<grid, kCpThreads, smem, as_stream(stream)>>>(
+      mst, static_cast<const __nv_bfloat16 *>(k), u, alpha, acc_nodes, n_acc, status, B, N, Hk,
+      Hv, dk, dv, state_out, stages);
   return launch_status();
 }
