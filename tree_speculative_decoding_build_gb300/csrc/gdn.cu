@@ -1111,9 +1111,9 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
 //             columns), by one round of asynchronous copies (the path itself
 //             is read when the sequence changes); under full memory load such a
 //             round takes microseconds, so one warp alone held the pipeline back;
-//   warps 4-11 per tile: read it, free its stage, then the new rows (thread:
-//             up to four 16-byte pieces of the tile), stored straight to
-//             global memory.
+//   warps 4-11 two halves of four warps, taking alternate tiles: read the
+//             tile, free its stage, then the new rows (thread: up to eight
+//             16-byte pieces of the tile), stored straight to global memory.
 // Every wait is bounded (2 s); a wait that runs out makes every role stop,
 // copies in flight get a bounded chance to land, and the rows of the tiles not
 // reached are left unwritten.
@@ -1163,7 +1163,7 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
   if (tid == 0) {
     for (int i = 0; i < stages; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&bars.empty[i]), kCpConsumers);
+      ptx::mbar_init(ptx::smem_u32(&bars.empty[i]), kCpConsumers / 2);  // one consumer half per tile
     }
     for (int i = 0; i < kCpSetupBufs; ++i) {
       ptx::mbar_init(ptx::smem_u32(&bars.setup_full[i]), 32);
@@ -1262,11 +1262,15 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
     // S_out = g_l S_0 + sum_p gam_p u_p[j] k_p, with gam_p (the product of
     // alpha over the path nodes after p) formed from the end of the path, and
     // g_l the product over all of it
-    const int ct = tid - 32 * (1 + kCpSetupBufs);
+    // two halves of the consumers take alternate tiles, so two tiles are in
+    // work at once
+    const int cid = tid - 32 * (1 + kCpSetupBufs);
+    const int half = cid / (kCpConsumers / 2), ct = cid - half * (kCpConsumers / 2);
+    constexpr int kHalf = kCpConsumers / 2;
     long long n = 0;
     int g = 0;
     bool ok = true;
-    constexpr int kIter = kGcDC * 128 / (kCpConsumers * 4);  // 16-byte pieces per thread (<= 4)
+    constexpr int kIter = kGcDC * 128 / (kHalf * 4);  // 16-byte pieces per thread (<= 8)
     for (long long gr = blockIdx.x; ok && gr < groups; gr += gridDim.x, ++g) {
       if (g > 0) ptx::mbar_arrive(ptx::smem_u32(&bars.setup_empty[(g - 1) % kCpSetupBufs]));
       const int sb = g % kCpSetupBufs;
@@ -1278,26 +1282,27 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
       const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(buf + 16 + gam_bytes);
       const float *us = reinterpret_cast<const float *>(buf + 16 + gam_bytes + (size_t)N * dk * 2);
       for (int c = 0; c < nC; ++c, ++n) {
+        if ((int)(n & 1) != half) continue;
         const int st = (int)(n % stages);
         if (!(ok = cp_wait(ptx::smem_u32(&bars.full[st]), (uint32_t)((n / stages) & 1), abort_flag))) break;
         const float *tl = reinterpret_cast<const float *>(smem + (uint32_t)st * kCpTileMax);
         float4 sv[kIter];
 #pragma unroll
         for (int i2 = 0; i2 < kIter; ++i2) {
-          const int e = (ct + i2 * kCpConsumers) * 4;
+          const int e = (ct + i2 * kHalf) * 4;
           if (e < kGcDC * dk) sv[i2] = *reinterpret_cast<const float4 *>(tl + e);
         }
         ptx::mbar_arrive(ptx::smem_u32(&bars.empty[st]));  // the stage may be refilled
         float *dst = state_out + (size_t)(gr * nC + c) * kGcDC * dk;
         // the path loop outside, the thread's pieces inside: their chains
         // interleave, and a piece's column of k is one load per node (the
-        // pieces of a thread lie in rows kCpConsumers * 4 / d_k apart, in the
-        // same columns when d_k divides kCpConsumers * 4)
+        // pieces of a thread lie in rows kHalf * 4 / d_k apart, in the same
+        // columns when d_k divides kHalf * 4)
         float4 acc[kIter];
         int jj[kIter], ii[kIter];
 #pragma unroll
         for (int i2 = 0; i2 < kIter; ++i2) {
-          const int e = (ct + i2 * kCpConsumers) * 4;
+          const int e = (ct + i2 * kHalf) * 4;
           jj[i2] = e / dk;
           ii[i2] = e - jj[i2] * dk;
           acc[i2] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1319,7 +1324,7 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
         }
 #pragma unroll
         for (int i2 = 0; i2 < kIter; ++i2) {
-          const int e = (ct + i2 * kCpConsumers) * 4;
+          const int e = (ct + i2 * kHalf) * 4;
           if (e >= kGcDC * dk) continue;
           __stcs(reinterpret_cast<float4 *>(dst + e),  // streamed: written once, not read back here
                  make_float4(fmaf(sv[i2].x, cur, acc[i2].x), fmaf(sv[i2].y, cur, acc[i2].y),
