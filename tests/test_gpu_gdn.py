@@ -132,7 +132,11 @@ def test_bad_tree_is_skipped(tv, kernel, kw):
     assert torch.isfinite(g[0]).all() and torch.isfinite(g[2]).all()
 
 
-@pytest.mark.parametrize("kw", [dict(), dict(B=3, N=32, Hk=4, Hv=8, dk=128, dv=128)])
+# d_k 32, 64 and 128 take the commit's shared-column loop (a thread's pieces in
+# the same columns), d_k 96 the general one
+@pytest.mark.parametrize("kw", [dict(), dict(B=3, N=32, Hk=4, Hv=8, dk=128, dv=128),
+                                dict(B=4, N=20, Hk=2, Hv=4, dk=64, dv=128),
+                                dict(B=3, N=24, Hk=1, Hv=2, dk=96, dv=64)])
 def test_commit_matches_oracle(tv, kw):
     x = to_dev(workloads.make_gdn("gdn_small", "cpu", **kw))
     out, u, g, st = run_verify(tv, x)

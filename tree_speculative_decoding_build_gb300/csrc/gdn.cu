@@ -1147,7 +1147,10 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
                        const int32_t *__restrict__ acc_nodes, const int32_t *__restrict__ n_acc,
                        const int32_t *__restrict__ status, int B, int N, int Hk, int Hv, int dk,
                        int dv, float *__restrict__ state_out, int stages) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  // the tiles are tensor-copy destinations (and sources): 128-byte aligned,
+  // whatever the static shared memory before the dynamic buffer
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = smem_raw + (((ptx::smem_u32(smem_raw) + 127u) & ~127u) - ptx::smem_u32(smem_raw));
   __shared__ CpBars bars;
   __shared__ int s_abort;
   __shared__ long long s_issued;  // state tiles the copy warp sent
@@ -1271,6 +1274,9 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
     int g = 0;
     bool ok = true;
     constexpr int kIter = kGcDC * 128 / (kHalf * 4);  // 16-byte pieces per thread (<= 8)
+    // the pieces of a thread lie kHalf * 4 elements apart: in the same columns
+    // when d_k divides that
+    const bool same_col = (kHalf * 4) % dk == 0;
     for (long long gr = blockIdx.x; ok && gr < groups; gr += gridDim.x, ++g) {
       if (g > 0) ptx::mbar_arrive(ptx::smem_u32(&bars.setup_empty[(g - 1) % kCpSetupBufs]));
       const int sb = g % kCpSetupBufs;
@@ -1308,19 +1314,37 @@ gdn_commit_pipe_kernel(const __grid_constant__ CUtensorMap tm_st, const __nv_bfl
           acc[i2] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float cur = 1.f;
-        for (int pp = L - 1; pp >= 0; --pp) {
-          const float *ur = us + (size_t)pp * dv + c * kGcDC;
-          const __nv_bfloat16 *kr = ks + (size_t)pp * dk;
+        if (same_col) {
+          // every piece of the thread reads the same four k values per node
+          for (int pp = L - 1; pp >= 0; --pp) {
+            const float *ur = us + (size_t)pp * dv + c * kGcDC;
+            const uint2 kw = *reinterpret_cast<const uint2 *>(ks + (size_t)pp * dk + ii[0]);
+            const float k0 = bf16_lo(kw.x), k1 = bf16_hi(kw.x), k2 = bf16_lo(kw.y), k3 = bf16_hi(kw.y);
 #pragma unroll
-          for (int i2 = 0; i2 < kIter; ++i2) {
-            const float up = cur * ur[jj[i2] < kGcDC ? jj[i2] : 0];
-            const uint2 kw = *reinterpret_cast<const uint2 *>(kr + ii[i2]);
-            acc[i2].x = fmaf(up, bf16_lo(kw.x), acc[i2].x);
-            acc[i2].y = fmaf(up, bf16_hi(kw.x), acc[i2].y);
-            acc[i2].z = fmaf(up, bf16_lo(kw.y), acc[i2].z);
-            acc[i2].w = fmaf(up, bf16_hi(kw.y), acc[i2].w);
+            for (int i2 = 0; i2 < kIter; ++i2) {
+              const float up = cur * ur[jj[i2] < kGcDC ? jj[i2] : 0];
+              acc[i2].x = fmaf(up, k0, acc[i2].x);
+              acc[i2].y = fmaf(up, k1, acc[i2].y);
+              acc[i2].z = fmaf(up, k2, acc[i2].z);
+              acc[i2].w = fmaf(up, k3, acc[i2].w);
+            }
+            cur *= al[pp];
           }
-          cur *= al[pp];
+        } else {
+          for (int pp = L - 1; pp >= 0; --pp) {
+            const float *ur = us + (size_t)pp * dv + c * kGcDC;
+            const __nv_bfloat16 *kr = ks + (size_t)pp * dk;
+#pragma unroll
+            for (int i2 = 0; i2 < kIter; ++i2) {
+              const float up = cur * ur[jj[i2] < kGcDC ? jj[i2] : 0];
+              const uint2 kw = *reinterpret_cast<const uint2 *>(kr + ii[i2]);
+              acc[i2].x = fmaf(up, bf16_lo(kw.x), acc[i2].x);
+              acc[i2].y = fmaf(up, bf16_hi(kw.x), acc[i2].y);
+              acc[i2].z = fmaf(up, bf16_lo(kw.y), acc[i2].z);
+              acc[i2].w = fmaf(up, bf16_hi(kw.y), acc[i2].w);
+            }
+            cur *= al[pp];
+          }
         }
 #pragma unroll
         for (int i2 = 0; i2 < kIter; ++i2) {
@@ -1474,7 +1498,7 @@ extern "C" tv_status tv_gdn_commit(const float *state_in, const void *k, const f
     return TV_ERR_ARG;
   const size_t setup = kCpSetupBufs * (size_t)cp_setup_bytes(N, dk, dv);
   const int stages = (int)std::min<size_t>(kCpStagesMax, (220u * 1024u - setup) / kCpTileMax);
-  const size_t smem = (size_t)stages * kCpTileMax + setup;
+  const size_t smem = (size_t)stages * kCpTileMax + setup + 128;  // + alignment slack
   if (cudaFuncSetAttribute(gdn_commit_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return TV_ERR_CUDA;
