@@ -905,20 +905,31 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
         const uint32_t kq = sb + (uint32_t)q * kPipeStage;
         const uint32_t d = tmem + kPipeColD;
         const uint32_t ap = tmem + kPipeColPlanes * (uint32_t)q;
-        for (int pl = 0; pl < 3; ++pl)
-          for (int kk = 0; kk < dk / 16; ++kk) {
-            const uint64_t bd = gdn_sw128_desc(kq + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u);
-            ptx::umma_f16_ta_warp(d, ap + (uint32_t)(pl * (dk / 2) + kk * 8), bd, idesc1,
-                                  (pl | kk) != 0 ? 1u : 0u);
-          }
-        // A = the [K; Q] tile read as 128 rows (rows past 64 are other data
-        // of the stage: rows of D2 nobody reads), B = its 32 K rows
-        for (int kk = 0; kk < dk / 16; ++kk) {
-          const uint64_t ad = gdn_sw128_desc(kq + (uint32_t)(kk >> 2) * 8192u + (uint32_t)(kk & 3) * 32u);
-          ptx::umma_f16_warp(d + 64, ad, ad, idesc2, kk != 0 ? 1u : 0u);
+        // the [K; Q] tile's descriptor; K step kk starts (kk >> 2) * 8192 +
+        // (kk & 3) * 32 bytes in (the same for the three planes and for D2),
+        // added to the descriptor's start field (shared addresses stay far
+        // below its 256 KB range).  One elected lane issues every MMA.
+        const int nkk = dk / 16;
+        const uint64_t kd0 = gdn_sw128_desc(kq);
+#define KD(kk) (kd0 + (uint64_t)((((kk) >> 2) * 8192 + ((kk) & 3) * 32) >> 4))
+        if (ptx::elect_one()) {
+#pragma unroll
+          for (int pl = 0; pl < 3; ++pl)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              if (kk < nkk)
+                ptx::umma_f16_ta(d, ap + (uint32_t)(pl * (dk / 2) + kk * 8), KD(kk), idesc1,
+                                 (pl | kk) != 0 ? 1u : 0u);
+          // A = the [K; Q] tile read as 128 rows (rows past 64 are other data
+          // of the stage: rows of D2 nobody reads), B = its 32 K rows
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            if (kk < nkk) ptx::umma_f16(d + 64, KD(kk), KD(kk), idesc2, kk != 0 ? 1u : 0u);
+          ptx::umma_commit(ptx::smem_u32(&bars.planes_empty[q]));
+          ptx::umma_commit(ptx::smem_u32(&bars.d_full[q]));
         }
-        ptx::umma_commit_warp(ptx::smem_u32(&bars.planes_empty[q]));
-        ptx::umma_commit_warp(ptx::smem_u32(&bars.d_full[q]));
+        __syncwarp();
+#undef KD
         issued_mma = k + 1;
       }
     }

@@ -153,6 +153,13 @@ __device__ __forceinline__ void umma_f16_ta_warp(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// true in one lane of a converged warp (elect.sync)
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(r));
+  return r != 0;
+}
+
 __device__ __forceinline__ void umma_commit_warp(uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
