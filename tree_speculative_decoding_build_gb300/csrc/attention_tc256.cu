@@ -283,29 +283,39 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   } else if (warp == 1) {
     // ============================================================ MMA issuer
     const uint32_t idesc_pv = idesc_f16(kM, kD, true);
+    // One elected lane issues a tile's MMAs and their commits (the same lane
+    // every time: elect.sync takes the lowest lane of the converged warp).
+    // The descriptors of the K steps and V blocks are the tile's base
+    // descriptor plus the step's offset in its start field (shared addresses
+    // stay below that field's 256 KB range).
     auto issue_s = [&](int j) {
       const int stage = j % kStages;
       const int keys = j < rg.n_ctx ? kBN : rg.np;
-      const uint32_t kbase = sbase + stage * kStageBytes;
-#pragma unroll 1
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint64_t bd = desc_sw128(kbase + (kk >> 2) * kQuarter + (kk & 3) * 32, 16);
-        umma_f16_ta_warp(tmem + kColS, tmem + kColQ + kk * 8, bd, idesc_f16(kM, keys, false),
-                         kk > 0 ? 1u : 0u);
+      const uint64_t bd0 = desc_sw128(sbase + stage * kStageBytes, 16);
+      const uint32_t id = idesc_f16(kM, keys, false);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          umma_f16_ta(tmem + kColS, tmem + kColQ + kk * 8,
+                      bd0 + (uint64_t)(((kk >> 2) * kQuarter + (kk & 3) * 32) >> 4), id, kk > 0 ? 1u : 0u);
+        umma_commit(smem_u32(&bars.s_full));
       }
-      umma_commit_warp(smem_u32(&bars.s_full));
+      __syncwarp();
     };
     auto issue_pv = [&](int j) {
       const int stage = j % kStages;
       const int nblk = j < rg.n_ctx ? 4 : rg.np / 16;
-      const uint32_t vbase = sbase + stage * kStageBytes + kKBytes;
-#pragma unroll 1
-      for (int i = 0; i < nblk; ++i) {
-        const uint64_t bd = desc_sw128(vbase + i * kBlkBytes, kBlkQuarter);
-        umma_f16_ta_warp(tmem + kColO, tmem + kColP + i * 8, bd, idesc_pv, (j > 0 || i > 0) ? 1u : 0u);
+      const uint64_t bd0 = desc_sw128(sbase + stage * kStageBytes + kKBytes, kBlkQuarter);
+      if (elect_one()) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nblk)
+            umma_f16_ta(tmem + kColO, tmem + kColP + i * 8, bd0 + (uint64_t)((i * kBlkBytes) >> 4), idesc_pv,
+                        (j > 0 || i > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&bars.pv_done));
+        umma_commit(smem_u32(&bars.kv_empty[stage]));
       }
-      umma_commit_warp(smem_u32(&bars.pv_done));
-      umma_commit_warp(smem_u32(&bars.kv_empty[stage]));
+      __syncwarp();
     };
     if (rg.n_tiles > 0) {
       ok = warp_wait(smem_u32(&bars.q_full), 0, abort_flag);

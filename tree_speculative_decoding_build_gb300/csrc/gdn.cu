@@ -46,13 +46,6 @@ constexpr int kGdnWarps = 8;
 constexpr int kGdnThreads = 32 * kGdnWarps;
 constexpr int kGdnMaxN = 64;
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t p;
-  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.b32 %0, 1, 0, e;\n\t}"
-               : "=r"(p));
-  return p != 0;
-}
-
 // 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all)
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
@@ -506,7 +499,7 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
   const uint32_t bar = ptx::smem_u32(&s_bar);
   // 3. the MMAs: one elected thread
   if (w == 0) {
-    if (elect_one()) {
+    if (ptx::elect_one()) {
       const uint32_t a0 = ptx::smem_u32(sA), b0 = ptx::smem_u32(sB);
       const uint32_t idesc = gdn_idesc(kTcM, kTcCols);
       for (int p = 0; p < 3; ++p)
