@@ -46,6 +46,13 @@ constexpr int kGdnWarps = 8;
 constexpr int kGdnThreads = 32 * kGdnWarps;
 constexpr int kGdnMaxN = 64;
 
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.b32 %0, 1, 0, e;\n\t}"
+               : "=r"(p));
+  return p != 0;
+}
+
 // 16-byte asynchronous global -> shared copy (completes at cp_async_wait_all)
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
@@ -499,7 +506,7 @@ gdn_tree_verify_tc_kernel(const float *__restrict__ state, const __nv_bfloat16 *
   const uint32_t bar = ptx::smem_u32(&s_bar);
   // 3. the MMAs: one elected thread
   if (w == 0) {
-    if (ptx::elect_one()) {
+    if (elect_one()) {
       const uint32_t a0 = ptx::smem_u32(sA), b0 = ptx::smem_u32(sB);
       const uint32_t idesc = gdn_idesc(kTcM, kTcCols);
       for (int p = 0; p < 3; ++p)
@@ -985,17 +992,24 @@ gdn_tree_verify_pipe_kernel(const __grid_constant__ CUtensorMap tm_s,
           const uint64_t msk = mc[t] & ((2ull << t) - 1);  // ancestors-or-self
           const float bt = mb[t];
           float *row = (qd == 0 ? X : Y) + t * kPipeXS;
-          float gam = 1.f;  // g_t / g_i, built from alpha going up the path
+          // the raw row first, then a short loop (not unrolled: its code is
+          // fetched once, not per problem) turns it into the row of X or Y in place
 #pragma unroll
+          for (int i0 = 0; i0 < kPipeN; i0 += 4)
+            *reinterpret_cast<uint4 *>(row + i0) = make_uint4(dot[i0], dot[i0 + 1], dot[i0 + 2], dot[i0 + 3]);
+          __syncwarp();
+          float gam = 1.f;  // g_t / g_i, built from alpha going up the path
+#pragma unroll 1
           for (int i0 = kPipeN - 4; i0 >= 0; i0 -= 4) {  // four columns at a time
             const float4 a4 = *reinterpret_cast<const float4 *>(ma + i0);
-            const float al[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float4 d4 = *reinterpret_cast<const float4 *>(row + i0);
+            const float al[4] = {a4.x, a4.y, a4.z, a4.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
             float rv[4];
 #pragma unroll
             for (int e = 3; e >= 0; --e) {
               const int i = i0 + e;
               const bool a = (msk >> i) & 1;
-              const float dv_i = gam * __uint_as_float(dot[i]);
+              const float dv_i = gam * dd[e];
               rv[e] = qd == 0 ? ((a && i != t) ? bt * dv_i : 0.f) : (a ? dv_i : 0.f);
               gam = a ? gam * al[e] : gam;
             }
