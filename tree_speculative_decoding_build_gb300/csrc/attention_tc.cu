@@ -977,8 +977,12 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
 // i % 128 and 32 dims.  The pieces are in CTAs c, c+1, ... up to the one whose
 // range holds the pair's last tile; slot 2d (a piece that starts a CTA's
 // range) or 2c + 1 (CTA c's piece, when the pair starts inside its range).
+// The range starts are read 32 CTAs at a time; the (max, sum) and data of up
+// to kCombBatch pieces are loaded together, then merged in piece order.
 // Launched as a programmatic dependent of the attention grid: it waits for
 // that grid's completion before any read.
+constexpr int kCombBatch = 2;
+
 __global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp, int P) {
   // the next attention launch may start now: it waits for this grid before it
   // touches the scratch read here
@@ -992,38 +996,60 @@ __global__ void __launch_bounds__(256) attn_tc_combine_kernel(const TcParams tp,
   const int pair = (int)(dsc.y >> 32);
   const int b = pair / p.Hkv, kvh = pair - b * p.Hkv;
   __shared__ long long s_lo[33];
+  __shared__ int s_slot[32];
+  __shared__ int s_n;
   const int m = threadIdx.x & 127, d0 = 64 * blockIdx.y + 32 * (threadIdx.x >> 7);
   float Mx = -INFINITY, Lx = 0.f, acc[32];
 #pragma unroll
   for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-  // windows of 32 CTAs: their range starts, then the pieces they hold
+  // windows of 32 CTAs: their range starts, the pieces they hold, then the
+  // pieces' partials kCombBatch at a time
   for (int w0 = c; w0 < P; w0 += 32) {
     __syncthreads();
     if (threadIdx.x < 33) s_lo[threadIdx.x] = w0 + (int)threadIdx.x <= P ? tp.lo_out[w0 + threadIdx.x] : E;
     __syncthreads();
-    bool done = false;
-    for (int i = 0; i < 32 && w0 + i < P; ++i) {
-      const int d = w0 + i;
-      const long long ld = s_lo[i], hd = s_lo[i + 1];
-      if (ld >= E) {
-        done = true;
-        break;
+    if (threadIdx.x == 0) {
+      int n = 0;
+      for (int i = 0; i < 32 && w0 + i < P; ++i) {
+        const int d = w0 + i;
+        const long long ld = s_lo[i], hd = s_lo[i + 1];
+        if (ld >= E) {
+          n = -1 - n;  // the pair ends in this window
+          break;
+        }
+        if (ld == hd) continue;  // an empty range holds no piece
+        s_slot[n++] = 2 * d + ((d == c && ld < S) ? 1 : 0);
       }
-      if (ld == hd) continue;  // an empty range holds no piece
-      const int slot = 2 * d + ((d == c && ld < S) ? 1 : 0);
-      if (!TV_CHECK(slot < 2 * P && d0 + 32 <= kD)) continue;
-      const float2 ml = __ldcg(tp.part_ml + (size_t)slot * kM + m);
-      const float *src = tp.part_o + ((size_t)slot * kD + d0) * kM + m;
-      float o[32];
+      s_n = n;
+    }
+    __syncthreads();
+    const int nraw = s_n;
+    const bool done = nraw < 0;
+    const int n = done ? -1 - nraw : nraw;
+    for (int i0 = 0; i0 < n; i0 += kCombBatch) {
+      float2 ml[kCombBatch];
+      float o[kCombBatch][32];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) o[k] = __ldcg(src + (size_t)k * kM);
-      if (ml.x == -INFINITY) continue;  // no key seen: O = 0
-      const float Mn = fmaxf(Mx, ml.x);
-      const float a = Mx == -INFINITY ? 0.f : exp2f(Mx - Mn), w = exp2f(ml.x - Mn);
-      Lx = Lx * a + ml.y * w;
+      for (int i = 0; i < kCombBatch; ++i) {
+        ml[i] = make_float2(-INFINITY, 0.f);
+        if (i0 + i < n && TV_CHECK(s_slot[i0 + i] < 2 * P && d0 + 32 <= kD)) {
+          const int slot = s_slot[i0 + i];
+          ml[i] = __ldcg(tp.part_ml + (size_t)slot * kM + m);
+          const float *src = tp.part_o + ((size_t)slot * kD + d0) * kM + m;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k] = acc[k] * a + o[k] * w;
-      Mx = Mn;
+          for (int k = 0; k < 32; ++k) o[i][k] = __ldcg(src + (size_t)k * kM);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kCombBatch; ++i) {
+        if (ml[i].x == -INFINITY) continue;  // no piece, or no key seen: O = 0
+        const float Mn = fmaxf(Mx, ml[i].x);
+        const float a = Mx == -INFINITY ? 0.f : exp2f(Mx - Mn), w = exp2f(ml[i].x - Mn);
+        Lx = Lx * a + ml[i].y * w;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] = acc[k] * a + o[i][k] * w;
+        Mx = Mn;
+      }
     }
     if (done) break;
   }
