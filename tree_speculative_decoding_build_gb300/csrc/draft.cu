@@ -461,6 +461,9 @@ topk_stream_kernel(const T *__restrict__ x, long long vpr, long long pen, long l
                    float *__restrict__ out_v, int32_t *__restrict__ out_i) {
   constexpr int E = 16 / sizeof(T);
   constexpr int kBatch = 32 * kTsUnroll;
+  // the merge grid may be launched now: it waits for this grid's completion
+  // before it reads the partial lists
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kTsWarps + (threadIdx.x >> 5);
   if (w >= owners) return;
@@ -584,7 +587,13 @@ topk_stream_kernel(const T *__restrict__ x, long long vpr, long long pen, long l
 }
 
 // Rows cut by range boundaries: warp p-1 of the grid owns boundary p when p is
-// the first boundary inside its row, and folds that row's pieces.
+// the first boundary inside its row, and folds that row's pieces.  Launched as
+// a programmatic dependent of the streaming grid: the boundary arithmetic and
+// the slots of the first kMergeHeld * 32 candidates are worked out while that
+// grid still runs; the pieces' lists are read after griddepcontrol.wait, the
+// held candidates all at once.
+constexpr int kMergeHeld = 4;
+
 __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
                                          const int32_t *__restrict__ part_i, long long vpr,
                                          long long pen, long long tot, long long owners, int k,
@@ -598,23 +607,47 @@ __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
   if (ts_split(p - 1, vpr, pen, tot, owners) > rs) return;  // an earlier boundary owns this row
   const long long c0 = p - 1;
   const long long c1 = ts_owner(rs + vpr - 1, vpr, pen, tot, owners);  // owner of the row's end
+  const long long total = (c1 - c0 + 1) * k;
+  // candidate qq is entry qq % k of piece c0 + qq / k: its pair's index in the
+  // partial arrays, or -1 when that piece's range is empty (nothing written)
+  auto cand = [&](long long qq) -> long long {
+    if (qq >= total) return -1;
+    const long long c = c0 + qq / k;
+    const int jj = (int)(qq - (qq / k) * k);
+    const long long s0 = ts_split(c, vpr, pen, tot, owners);
+    if (s0 == ts_split(c + 1, vpr, pen, tot, owners)) return -1;
+    return (2 * c + ((c == c0 && s0 < rs) ? 1 : 0)) * k + jj;
+  };
+  long long held[kMergeHeld];
+#pragma unroll
+  for (int h = 0; h < kMergeHeld; ++h) held[h] = cand(32LL * h + lane);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  float hv[kMergeHeld];
+  int hi[kMergeHeld];
+#pragma unroll
+  for (int h = 0; h < kMergeHeld; ++h) {
+    hv[h] = held[h] >= 0 ? part_v[held[h]] : -INFINITY;
+    hi[h] = held[h] >= 0 ? part_i[held[h]] : INT32_MAX;
+  }
   // the pieces' lists, 32 candidates per step, one per lane, folded into the
   // list at once (steps where none beats the k-th entry are skipped)
   float lv = -INFINITY, tv = -INFINITY;
   int li = INT32_MAX, ti = INT32_MAX;
-  const long long total = (c1 - c0 + 1) * k;
   for (long long q0 = 0; q0 < total; q0 += 32) {
-    const long long qq = q0 + lane;
+    const int h = (int)(q0 / 32);
     float x = -INFINITY;
     int xi = INT32_MAX;
-    if (qq < total) {
-      const long long c = c0 + qq / k;
-      const int jj = (int)(qq - (qq / k) * k);
-      const long long s0 = ts_split(c, vpr, pen, tot, owners);
-      if (s0 != ts_split(c + 1, vpr, pen, tot, owners)) {  // empty ranges wrote nothing
-        const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
-        x = part_v[slot * k + jj];
-        xi = part_i[slot * k + jj];
+#pragma unroll
+    for (int e = 0; e < kMergeHeld; ++e)
+      if (e == h) {
+        x = hv[e];
+        xi = hi[e];
+      }
+    if (h >= kMergeHeld) {  // rows cut into more pieces than held
+      const long long o = cand(q0 + lane);
+      if (o >= 0) {
+        x = part_v[o];
+        xi = part_i[o];
       }
     }
     if (!__any_sync(0xffffffffu, xi != INT32_MAX && beats(x, xi, tv, ti))) continue;
@@ -909,8 +942,19 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
       topk_stream_kernel<float><<<p.ctas, 32 * kTsWarps, 0, s>>>(
           static_cast<const float *>(x), vpr, pen, tot, owners, k, pv, pi, out_vals, out_idx);
     const int wpb = 8;
-    topk_stream_merge_kernel<<<(unsigned)((owners - 1 + wpb - 1) / wpb), 32 * wpb, 0, s>>>(
-        pv, pi, vpr, pen, tot, owners, k, out_vals, out_idx);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)((owners - 1 + wpb - 1) / wpb));
+    cfg.blockDim = dim3(32 * wpb);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, topk_stream_merge_kernel, static_cast<const float *>(pv),
+                           static_cast<const int32_t *>(pi), vpr, pen, tot, owners, k, out_vals,
+                           out_idx) != cudaSuccess)
+      return TV_ERR_CUDA;
     return launch_status();
   }
   const bool vec = ((reinterpret_cast<uintptr_t>(x) & 15) == 0) && ((row_stride * esize) % 16 == 0);
