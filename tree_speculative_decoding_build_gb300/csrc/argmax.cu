@@ -249,6 +249,9 @@ argmax_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long 
                      int32_t *__restrict__ out_idx) {
   constexpr int E = 16 / sizeof(T);
   constexpr int kBatch = 32 * kStrUnroll;
+  // the merge grid may be launched now: it waits for this grid's completion
+  // before it reads the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kStrWarps + (threadIdx.x >> 5);
   if (w >= owners) return;
@@ -329,6 +332,8 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
                                            const int32_t *__restrict__ part_i, long long nv,
                                            long long vpr, long long owners,
                                            int32_t *__restrict__ out_idx) {
+  // launched as a programmatic dependent of the streaming grid: the partials
+  // are read after griddepcontrol.wait
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5) + 1;
   const int lane = threadIdx.x & 31;
   if (p >= owners) return;
@@ -340,13 +345,21 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
   // owner of the row's last vector x: ceil((x+1) * owners / nv) - 1
   const long long xl = rs + vpr - 1;
   const long long c1 = ((xl + 1) * owners + nv - 1) / nv - 1;
-  Best me{-INFINITY, INT32_MAX};
-  for (long long c = c0 + lane; c <= c1; c += 32) {
+  // the slot of this lane's piece (or -1: none, or an empty range that wrote
+  // nothing), worked out before the streaming grid has finished
+  auto slot_of = [&](long long c) -> long long {
+    if (c > c1 || !TV_CHECK(c < owners)) return -1;
     const long long s0 = str_split(c, nv, owners);
-    if (s0 == str_split(c + 1, nv, owners)) continue;  // empty range
-    const long long slot = 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
-    if (!TV_CHECK(c < owners)) continue;
-    merge(me, Best{part_v[slot], part_i[slot]});
+    if (s0 == str_split(c + 1, nv, owners)) return -1;
+    return 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
+  };
+  const long long first = slot_of(c0 + lane);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  Best me{-INFINITY, INT32_MAX};
+  if (first >= 0) merge(me, Best{part_v[first], part_i[first]});
+  for (long long c = c0 + lane + 32; c <= c1; c += 32) {  // rows cut into more than 32 pieces
+    const long long slot = slot_of(c);
+    if (slot >= 0) merge(me, Best{part_v[slot], part_i[slot]});
   }
   me = warp_best(me);
   if (lane == 0 && TV_CHECK(r < nv / vpr && me.i >= 0 && me.i < vpr * (16 / 2))) out_idx[r] = me.i;
@@ -416,8 +429,18 @@ tv_status launch_argmax(const void *logits, int dtype, long long rows, long long
       argmax_stream_kernel<float><<<p.ctas, kStrThreads, 0, s>>>(
           static_cast<const float *>(logits), nv, vpr, owners, pv, pi, out_idx);
     const int wpb = 8;
-    argmax_stream_merge_kernel<<<(unsigned)((owners - 1 + wpb - 1) / wpb), wpb * 32, 0, s>>>(
-        pv, pi, nv, vpr, owners, out_idx);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3((unsigned)((owners - 1 + wpb - 1) / wpb));
+    cfg.blockDim = dim3(wpb * 32);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, argmax_stream_merge_kernel, static_cast<const float *>(pv),
+                           static_cast<const int32_t *>(pi), nv, vpr, owners, out_idx) != cudaSuccess)
+      return TV_ERR_CUDA;
     return launch_status();
   }
   const bool vec = ((reinterpret_cast<uintptr_t>(logits) & 15) == 0) &&
