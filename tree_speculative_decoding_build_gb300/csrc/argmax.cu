@@ -250,8 +250,10 @@ argmax_stream_kernel(const T *__restrict__ x, long long nv, long long vpr, long 
   constexpr int E = 16 / sizeof(T);
   constexpr int kBatch = 32 * kStrUnroll;
   // the merge grid may be launched now: it waits for this grid's completion
-  // before it reads the partials
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // before it reads the partials.  (This grid itself is launched normally: as
+  // a programmatic dependent of the attention's combine grid the verify step
+  // took 22 us longer.)
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kStrWarps + (threadIdx.x >> 5);
   if (w >= owners) return;
@@ -333,7 +335,9 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
                                            long long vpr, long long owners,
                                            int32_t *__restrict__ out_idx) {
   // launched as a programmatic dependent of the streaming grid: the partials
-  // are read after griddepcontrol.wait
+  // are read after griddepcontrol.wait; the grid after this one (the tree
+  // walk) may be scheduled at once
+  pdl_launch_dependents();
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5) + 1;
   const int lane = threadIdx.x & 31;
   if (p >= owners) return;
@@ -354,7 +358,7 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
     return 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
   };
   const long long first = slot_of(c0 + lane);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
   Best me{-INFINITY, INT32_MAX};
   if (first >= 0) merge(me, Best{part_v[first], part_i[first]});
   for (long long c = c0 + lane + 32; c <= c1; c += 32) {  // rows cut into more than 32 pieces
@@ -429,17 +433,8 @@ tv_status launch_argmax(const void *logits, int dtype, long long rows, long long
       argmax_stream_kernel<float><<<p.ctas, kStrThreads, 0, s>>>(
           static_cast<const float *>(logits), nv, vpr, owners, pv, pi, out_idx);
     const int wpb = 8;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)((owners - 1 + wpb - 1) / wpb));
-    cfg.blockDim = dim3(wpb * 32);
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, argmax_stream_merge_kernel, static_cast<const float *>(pv),
-                           static_cast<const int32_t *>(pi), nv, vpr, owners, out_idx) != cudaSuccess)
+    if (launch_pdl(argmax_stream_merge_kernel, dim3((unsigned)((owners - 1 + wpb - 1) / wpb)),
+                   dim3(wpb * 32), 0, s, pv, pi, nv, vpr, owners, out_idx) != cudaSuccess)
       return TV_ERR_CUDA;
     return launch_status();
   }

@@ -463,7 +463,7 @@ topk_stream_kernel(const T *__restrict__ x, long long vpr, long long pen, long l
   constexpr int kBatch = 32 * kTsUnroll;
   // the merge grid may be launched now: it waits for this grid's completion
   // before it reads the partial lists
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * kTsWarps + (threadIdx.x >> 5);
   if (w >= owners) return;
@@ -621,7 +621,7 @@ __global__ void topk_stream_merge_kernel(const float *__restrict__ part_v,
   long long held[kMergeHeld];
 #pragma unroll
   for (int h = 0; h < kMergeHeld; ++h) held[h] = cand(32LL * h + lane);
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
   float hv[kMergeHeld];
   int hi[kMergeHeld];
 #pragma unroll
@@ -942,18 +942,9 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
       topk_stream_kernel<float><<<p.ctas, 32 * kTsWarps, 0, s>>>(
           static_cast<const float *>(x), vpr, pen, tot, owners, k, pv, pi, out_vals, out_idx);
     const int wpb = 8;
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)((owners - 1 + wpb - 1) / wpb));
-    cfg.blockDim = dim3(32 * wpb);
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_stream_merge_kernel, static_cast<const float *>(pv),
-                           static_cast<const int32_t *>(pi), vpr, pen, tot, owners, k, out_vals,
-                           out_idx) != cudaSuccess)
+    if (launch_pdl(topk_stream_merge_kernel, dim3((unsigned)((owners - 1 + wpb - 1) / wpb)),
+                   dim3(32 * wpb), 0, s, pv, pi, vpr, pen, tot, owners, k, out_vals, out_idx) !=
+        cudaSuccess)
       return TV_ERR_CUDA;
     return launch_status();
   }

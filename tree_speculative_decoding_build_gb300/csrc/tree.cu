@@ -54,7 +54,7 @@ __global__ void build_ancestors_kernel(const int32_t *__restrict__ parent,
                                        int32_t *__restrict__ status) {
   // the tree-attention grids launched after this one may start at once: they
   // wait for this grid's completion before reading anc / pos / status
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_launch_dependents();
   const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -95,6 +95,10 @@ __global__ void tree_walk_kernel(const int32_t *__restrict__ tokens,
                                  const int32_t *__restrict__ status, int B, int N,
                                  int32_t *__restrict__ out_tokens, int32_t *__restrict__ n_emit,
                                  int32_t *__restrict__ acc_nodes, int32_t *__restrict__ n_acc) {
+  // launched as a programmatic dependent: the commit grid after it may be
+  // scheduled now; this grid's inputs are read after the wait
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ int32_t path[4][kMaxNodes + 1];
   const int w = threadIdx.x >> 5;
   const int b = blockIdx.x * (blockDim.x >> 5) + w;
@@ -149,6 +153,8 @@ __global__ void commit_kv_kernel(const uint4 *__restrict__ k_tree, const uint4 *
                                  int D, int max_blocks, int num_blocks, uint4 *__restrict__ k_cache,
                                  uint4 *__restrict__ v_cache, int32_t *__restrict__ ctx_len_out,
                                  int32_t *__restrict__ status) {
+  pdl_launch_dependents();  // the next layer's commit may be scheduled now
+  pdl_wait();               // this grid's inputs are read after the wait
   const int b = blockIdx.x;
   __shared__ int32_t s_blk[kMaxNodes];
   __shared__ int32_t s_node[kMaxNodes];
@@ -235,8 +241,10 @@ extern "C" tv_status tv_tree_walk(const int32_t *tokens, const int32_t *parent,
   if (!root_pred || !out_tokens || !n_emit || !n_acc) return TV_ERR_ARG;
   if (N > 0 && (!tokens || !parent || !argmax || !acc_nodes)) return TV_ERR_ARG;
   const int warps = 4;
-  tree_walk_kernel<<<(B + warps - 1) / warps, warps * 32, 0, as_stream(stream)>>>(
-      tokens, parent, argmax, root_pred, status, B, N, out_tokens, n_emit, acc_nodes, n_acc);
+  if (launch_pdl(tree_walk_kernel, dim3((B + warps - 1) / warps), dim3(warps * 32), 0,
+                 as_stream(stream), tokens, parent, argmax, root_pred, status, B, N, out_tokens,
+                 n_emit, acc_nodes, n_acc) != cudaSuccess)
+    return TV_ERR_CUDA;
   return launch_status();
 }
 
@@ -256,10 +264,12 @@ extern "C" tv_status tv_commit_kv(const void *k_tree, const void *v_tree, const 
   if ((reinterpret_cast<uintptr_t>(k_tree) | reinterpret_cast<uintptr_t>(v_tree) |
        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
     return TV_ERR_ARG;
-  commit_kv_kernel<<<B, 256, 0, as_stream(stream)>>>(
-      static_cast<const uint4 *>(k_tree), static_cast<const uint4 *>(v_tree), acc_nodes, n_acc,
-      ctx_len_in, block_table, N, Hkv, D, max_blocks, num_blocks, static_cast<uint4 *>(k_cache),
-      static_cast<uint4 *>(v_cache), ctx_len_out, status);
+  if (launch_pdl(commit_kv_kernel, dim3(B), dim3(256), 0, as_stream(stream),
+                 static_cast<const uint4 *>(k_tree), static_cast<const uint4 *>(v_tree), acc_nodes,
+                 n_acc, ctx_len_in, block_table, N, Hkv, D, max_blocks, num_blocks,
+                 static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), ctx_len_out,
+                 status) != cudaSuccess)
+    return TV_ERR_CUDA;
   return launch_status();
 }
 
