@@ -230,8 +230,40 @@ __device__ __forceinline__ void take_own(bool flag, const uint4 &q, int idx0, in
   }
 }
 
-// The warp's list at the end of a block: warp 0 folds the other warps' k best
-// into its own and returns the block's k best in its lanes 0 .. k-1.
+// One compare-exchange step of a 32-lane network over (value, index) pairs:
+// this lane ends up with the better pair when keep_better, else the worse.
+__device__ __forceinline__ void cx_step(float &v, int &i, int stride, bool keep_better) {
+  const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+  const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
+  if (keep_better ? beats(ov, oi, v, i) : beats(v, i, ov, oi)) {
+    v = ov;
+    i = oi;
+  }
+}
+
+// Fold 32 candidates, one per lane, into the warp's sorted list (lane 0 the
+// best): bitonic sort of the candidates into ascending order, the better of
+// list[j] and candidate[j] in each lane (the 32 best of both, a bitonic
+// sequence), then a bitonic merge back into descending order.
+__device__ __forceinline__ void fold32(float &lv, int &li, float cv, int ci) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1)
+      // ascending blocks where lane & size == 0 (all of them at size 32)
+      cx_step(cv, ci, stride, ((lane & stride) != 0) == ((lane & size) == 0));
+  if (beats(cv, ci, lv, li)) {
+    lv = cv;
+    li = ci;
+  }
+#pragma unroll
+  for (int stride = 16; stride > 0; stride >>= 1) cx_step(lv, li, stride, (lane & stride) == 0);
+}
+
+// The warp's list at the end of a block: warp 0 folds the warps' k best
+// (kTopWarps * k candidates, 32 at a time) and returns the block's k best in
+// its lanes 0 .. k-1.
 __device__ __forceinline__ void block_fold(float &lv, int &li, int k) {
   __shared__ float sv[kTopWarps][32];
   __shared__ int si[kTopWarps][32];
@@ -240,13 +272,20 @@ __device__ __forceinline__ void block_fold(float &lv, int &li, int k) {
   si[w][lane] = li;
   __syncthreads();
   if (w == 0) {
-    for (int o = 1; o < kTopWarps; ++o)
-      for (int j = 0; j < k; ++j) {
-        const float x = sv[o][j];
-        const int xi = si[o][j];
-        if (xi == INT32_MAX) break;  // the rest of that list is empty
-        wl_insert(lv, li, x, xi);
+    float fv = -INFINITY;
+    int fi = INT32_MAX;
+    for (int q0 = 0; q0 < kTopWarps * k; q0 += 32) {
+      const int j = q0 + lane;
+      float x = -INFINITY;
+      int xi = INT32_MAX;
+      if (j < kTopWarps * k) {
+        x = sv[j / k][j % k];
+        xi = si[j / k][j % k];
       }
+      fold32(fv, fi, x, xi);
+    }
+    lv = fv;
+    li = fi;
   }
 }
 
@@ -258,6 +297,7 @@ template <typename T>
 __global__ void __launch_bounds__(kTopThreads)
 topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chunks, int chunk_len,
                   bool vec, int k, float *__restrict__ out_v, int32_t *__restrict__ out_i) {
+  pdl_launch_dependents();  // the merge grid may be scheduled now: it waits for this one
   constexpr int E = 16 / sizeof(T);
   const long long row = blockIdx.x / chunks;
   const int c = blockIdx.x - (int)(row * chunks);
@@ -349,24 +389,57 @@ topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chun
   }
 }
 
-// One warp per row: fold the row's chunks * k candidates into one list.
-__global__ void topk_merge_kernel(const float *__restrict__ part_v, const int32_t *__restrict__ part_i,
-                                  long long rows, int chunks, int k, float *__restrict__ out_v,
-                                  int32_t *__restrict__ out_i) {
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
+// One block per row: its warps fold the row's chunks * k candidates (warp w a
+// w-th share, 32 at a time), then warp 0 folds the warps' k best.  Launched as
+// a programmatic dependent of the chunk grid: the partials are read after the
+// wait.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps)
+topk_merge_kernel(const float *__restrict__ part_v, const int32_t *__restrict__ part_i,
+                  long long rows, int chunks, int k, float *__restrict__ out_v,
+                  int32_t *__restrict__ out_i) {
+  pdl_wait();
+  __shared__ float sv[kMergeWarps][32];
+  __shared__ int si[kMergeWarps][32];
+  const long long row = blockIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int n = chunks * k;
-  float lv = -INFINITY;
-  int li = INT32_MAX;
-  for (int j = 0; j < n; ++j) {
-    const int xi = part_i[row * n + j];
-    if (xi == INT32_MAX) continue;
-    wl_insert(lv, li, part_v[row * n + j], xi);
+  const int j0 = (int)((long long)n * w / kMergeWarps), j1 = (int)((long long)n * (w + 1) / kMergeWarps);
+  float lv = -INFINITY, tv = -INFINITY;
+  int li = INT32_MAX, ti = INT32_MAX;
+  for (int q0 = j0; q0 < j1; q0 += 32) {
+    const int j = q0 + lane;
+    float x = -INFINITY;
+    int xi = INT32_MAX;
+    if (j < j1) {
+      x = part_v[row * n + j];
+      xi = part_i[row * n + j];
+    }
+    if (!__any_sync(0xffffffffu, xi != INT32_MAX && beats(x, xi, tv, ti))) continue;
+    fold32(lv, li, x, xi);
+    tv = __shfl_sync(0xffffffffu, lv, k - 1);
+    ti = __shfl_sync(0xffffffffu, li, k - 1);
+  }
+  sv[w][lane] = lv;
+  si[w][lane] = li;
+  __syncthreads();
+  if (w != 0) return;
+  float fv = -INFINITY;
+  int fi = INT32_MAX;
+  for (int q0 = 0; q0 < kMergeWarps * k; q0 += 32) {  // the warps' k best, 32 at a time
+    const int j = q0 + lane;
+    float x = -INFINITY;
+    int xi = INT32_MAX;
+    if (j < kMergeWarps * k) {
+      x = sv[j / k][j % k];
+      xi = si[j / k][j % k];
+    }
+    fold32(fv, fi, x, xi);
   }
   if (lane < k) {
-    out_v[row * k + lane] = lv;
-    out_i[row * k + lane] = li;
+    out_v[row * k + lane] = fv;
+    out_i[row * k + lane] = fi;
   }
 }
 
@@ -420,37 +493,6 @@ __device__ __forceinline__ long long ts_owner(long long x, long long vpr, long l
   const long long row = x / vpr;
   const long long y = row * (vpr + pen) + pen + (x - row * vpr);
   return ((y + 1) * owners + tot - 1) / tot - 1;  // ceil((y + 1) * owners / tot) - 1
-}
-
-// One compare-exchange step of a 32-lane network over (value, index) pairs:
-// this lane ends up with the better pair when keep_better, else the worse.
-__device__ __forceinline__ void cx_step(float &v, int &i, int stride, bool keep_better) {
-  const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
-  const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
-  if (keep_better ? beats(ov, oi, v, i) : beats(v, i, ov, oi)) {
-    v = ov;
-    i = oi;
-  }
-}
-
-// Fold 32 candidates, one per lane, into the warp's sorted list (lane 0 the
-// best): bitonic sort of the candidates into ascending order, the better of
-// list[j] and candidate[j] in each lane (the 32 best of both, a bitonic
-// sequence), then a bitonic merge back into descending order.
-__device__ __forceinline__ void fold32(float &lv, int &li, float cv, int ci) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1)
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1)
-      // ascending blocks where lane & size == 0 (all of them at size 32)
-      cx_step(cv, ci, stride, ((lane & stride) != 0) == ((lane & size) == 0));
-  if (beats(cv, ci, lv, li)) {
-    lv = cv;
-    li = ci;
-  }
-#pragma unroll
-  for (int stride = 16; stride > 0; stride >>= 1) cx_step(lv, li, stride, (lane & stride) == 0);
 }
 
 template <typename T>
@@ -683,11 +725,12 @@ bool topk_stream_shape(long long rows, long long V, int esize) {
 
 TopkPlan topk_chunk_plan(long long rows, long long V, int esize, int k) {
   const int E = 16 / esize;
-  // a few thread blocks per SM; never cut a row below 32K elements
+  // a few thread blocks per SM; never cut a row below 4K elements (a warp's
+  // share then fits in one round of loads)
   const long long want = 8LL * sm_count();
   long long chunks = 1;
   if (rows < want) chunks = (want + rows - 1) / rows;
-  const long long max_chunks = (V + 32767) / 32768;
+  const long long max_chunks = (V + 4095) / 4096;
   if (chunks > max_chunks) chunks = max_chunks;
   if (chunks < 1) chunks = 1;
   long long len = (V + chunks - 1) / chunks;
@@ -960,11 +1003,10 @@ extern "C" tv_status tv_topk(const void *x, int dtype, int64_t rows, int64_t V, 
     topk_chunk_kernel<float><<<grid, kTopThreads, 0, s>>>(static_cast<const float *>(x), (int)V,
                                                           row_stride, p.chunks, p.chunk_len, vec, k,
                                                           cv, ci);
-  if (p.chunks > 1) {
-    const int wpb = 8;
-    topk_merge_kernel<<<(unsigned)((rows + wpb - 1) / wpb), 32 * wpb, 0, s>>>(pv, pi, rows, p.chunks,
-                                                                            k, out_vals, out_idx);
-  }
+  if (p.chunks > 1 &&
+      launch_pdl(topk_merge_kernel, dim3((unsigned)rows), dim3(32 * kMergeWarps), 0, s, pv, pi, rows,
+                 p.chunks, k, out_vals, out_idx) != cudaSuccess)
+    return TV_ERR_CUDA;
   return launch_status();
 }
 
