@@ -24,6 +24,16 @@
  *     caches that array's device address per device (see its comment).
  *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL means the
  *     legacy default stream) and never synchronises with the host.
+ *   - Stream order holds as usual.  Some kernels are launched as programmatic
+ *     dependents (tv_tree_attention, tv_tree_walk, tv_commit_kv and the merge
+ *     kernels of tv_argmax and tv_topk): they may become resident while the
+ *     kernel before them is still running, but only when that kernel is one of
+ *     this library's that releases its dependents early, and they read what
+ *     that kernel writes only after it has completed.  tv_tree_attention reads
+ *     q, the tree K/V, the KV cache and the block table early; none of this
+ *     library's kernels that release their dependents early writes any of
+ *     those (tv_commit_kv, which writes the cache, releases nothing early), and
+ *     a caller's own kernel releases nothing early, so stream order applies.
  *   - The return value reports argument/shape validation and launch errors
  *     only.  Data errors found on the device (a malformed tree, a bad block id)
  *     are written to the per-sequence `status` array (int32 [B]): 0 = ok, else a

@@ -40,10 +40,12 @@ def run_topk(tv, x, k):
 
 # (16, 262144), (64, 65536), (999, 3000) and (40000, 64) take the streaming
 # plan (rows cut between warp ranges, many rows per load batch); the others the
-# chunk plan.
+# chunk plan.  (4, 262144, 4) is the top-W proposer's shape (64 chunks a row);
+# (2, 262144, 16) folds 1024 candidates per row in the merge.
 @pytest.mark.parametrize("rows,V,k", [(1, 1, 1), (3, 7, 7), (8, 1024, 4), (16, 262144, 4),
                                       (5, 100003, 16), (300, 4099, 10), (1, 40000, 16),
-                                      (64, 65536, 10), (999, 3000, 10), (40000, 64, 16)])
+                                      (64, 65536, 10), (999, 3000, 10), (40000, 64, 16),
+                                      (4, 262144, 4), (2, 262144, 16)])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_topk_matches_oracle(tv, rows, V, k, dtype):
     g = torch.Generator(device="cuda").manual_seed(rows * 31 + V + k)

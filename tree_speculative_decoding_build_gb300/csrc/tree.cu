@@ -153,8 +153,10 @@ __global__ void commit_kv_kernel(const uint4 *__restrict__ k_tree, const uint4 *
                                  int D, int max_blocks, int num_blocks, uint4 *__restrict__ k_cache,
                                  uint4 *__restrict__ v_cache, int32_t *__restrict__ ctx_len_out,
                                  int32_t *__restrict__ status) {
-  pdl_launch_dependents();  // the next layer's commit may be scheduled now
-  pdl_wait();               // this grid's inputs are read after the wait
+  // this grid's inputs are read after the wait.  It releases no dependent
+  // early: a tree-attention grid launched after it reads the KV cache (which
+  // this grid writes) before its own wait.
+  pdl_wait();
   const int b = blockIdx.x;
   __shared__ int32_t s_blk[kMaxNodes];
   __shared__ int32_t s_node[kMaxNodes];
