@@ -236,6 +236,43 @@ def test_commit_matches_oracle_every_length(tv):
     assert np.array_equal(st.cpu().numpy(), rst)
 
 
+def test_attention_right_after_commit_reads_the_committed_rows(tv):
+    """tv_commit_kv followed at once (same stream, no ancestor pass between) by
+    tv_tree_attention over a context that now includes the rows just committed.
+    The attention kernel reads the KV cache before its own dependency wait, so
+    this holds only because the commit releases no dependent early."""
+    inp = workloads.make("best_first", "cuda", 21, B=4, ctx=(300, 700), V=64)
+    B, N = inp["B"], inp["N"]
+    n_acc = np.array([5, 8, 0, 3], np.int32)       # at most the workload's max depth (8)
+    acc = np.full((B, N), -1, np.int32)
+    for b in range(B):
+        acc[b, :n_acc[b]] = (np.arange(n_acc[b]) * 3 + b) % N
+    npi = workloads.to_numpy(inp)
+    ctx2 = (npi["ctx_len"] + n_acc).astype(np.int32)
+    anc = torch.empty((B, N), dtype=torch.int64, device="cuda")
+    pos = torch.empty((B, N), dtype=torch.int32, device="cuda")
+    st = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ctx2_d, ctx_out = dev_i32(ctx2), torch.empty(B, dtype=torch.int32, device="cuda")
+    kc, vc = inp["k_cache"].clone(), inp["v_cache"].clone()
+    out = torch.empty_like(inp["q"])
+    # the ancestors of the next step first, then the commit, then at once the attention
+    tv.tv_build_ancestors(inp["parent"], inp["depth"], ctx2_d, anc, pos, st)
+    tv.tv_commit_kv(inp["k_tree"], inp["v_tree"], dev_i32(acc), dev_i32(n_acc), inp["ctx_len"],
+                    inp["block_table"], kc, vc, ctx_out, st)
+    tv.tv_tree_attention(inp["q"], inp["k_tree"], inp["v_tree"], kc, vc, inp["block_table"], ctx2_d,
+                         pos, anc, out, st, window_left=inp["window_left"])
+    torch.cuda.synchronize()
+    assert np.array_equal(st.cpu().numpy(), np.zeros(B, np.int32))
+    assert np.array_equal(ctx_out.cpu().numpy(), ctx2)
+    rk, rv, _, _ = oracle.commit(npi["k_tree"], npi["v_tree"], acc, n_acc, npi["ctx_len"],
+                                 npi["block_table"], npi["k_cache"], npi["v_cache"])
+    ref_in = dict(npi)
+    ref_in["k_cache"] = rk.view(np.uint16)
+    ref_in["v_cache"] = rv.view(np.uint16)
+    ref_in["ctx_len"] = ctx2
+    assert_close(bf16_to_f64(out), oracle_attention(ref_in), "attention after commit")
+
+
 def test_commit_bad_blocks(tv):
     inp = workloads.make("tiny", "cuda", 4, B=3, ctx=(31, 31), N=4, tree="chain", V=64)
     npi = workloads.to_numpy(inp)
