@@ -785,20 +785,37 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
 #pragma unroll
           for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
         const float mxs = mt[0] * qscale;
-        // Rescale this warpgroup's O only when some row's max grew by more than
-        // 2^kTau; decided per warp (tcgen05.ld/st are warp-collective), rows
-        // that do not need it scale by 1.  A finite running max means this
-        // warpgroup had an earlier tile in the segment: PV_{j-2} wrote O last.
         const bool need = m_used != -INFINITY && mxs > m_used + kTau;
+        // the factor for O and l, and the new running max (raised to this
+        // tile's max when the old one is too low by 2^kTau, or set by the
+        // first tile); a running max of -inf means every score so far is
+        // -inf: 2^(-inf) = 0
+        const float alpha = need ? ex2(m_used - mxs) : 1.f;
+        const float m_new = (need || m_used == -INFINITY) ? mxs : m_used;
+        const float neg_m = m_new != -INFINITY ? -m_new : 0.f;
+        // P_j and its row sum need only the new max: they are formed while
+        // PV_{j-2} may still run
+        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float p0 = ex2(fmaf(s[c], qscale, neg_m));
+          const float p1 = ex2(fmaf(s[c + 1], qscale, neg_m));
+          ps[(c >> 1) & 7] += p0 + p1;
+          pk[c >> 1] = pack_bf16(p0, p1);
+        }
         if (j >= 2) {
           // PV_{j-2} done: P buffer x is free and O_x is quiescent
           ok = __all_sync(0xffffffffu, wait_fast(smem_u32(&bars.pv_done[x]),
                                                  (uint32_t)(((j - 2) >> 1) & 1), abort_flag));
           if (!ok) break;
         }
+        // Rescale this warpgroup's O only when some row's max grew by more than
+        // 2^kTau; decided per warp (tcgen05.ld/st are warp-collective), rows
+        // that do not need it scale by 1.  A finite running max means this
+        // warpgroup had an earlier tile in the segment: PV_{j-2} wrote O last.
         if (__any_sync(0xffffffffu, need)) {
           tc_fence_after();
-          const float alpha = need ? ex2(m_used - mxs) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             uint32_t o[32];
@@ -809,23 +826,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
             tmem_st32(t_o + c * 32, o);
           }
           tmem_wait_st();
-          if (need) {
-            l *= alpha;
-            m_used = mxs;
-          }
         }
-        if (m_used == -INFINITY) m_used = mxs;
-        // a running max of -inf means every score so far is -inf: 2^(-inf) = 0
-        const float neg_m = m_used != -INFINITY ? -m_used : 0.f;
-        float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float p0 = ex2(fmaf(s[c], qscale, neg_m));
-          const float p1 = ex2(fmaf(s[c + 1], qscale, neg_m));
-          ps[(c >> 1) & 7] += p0 + p1;
-          pk[c >> 1] = pack_bf16(p0, p1);
-        }
+        if (need) l *= alpha;
+        m_used = m_new;
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
         // P_j as bf16 pairs into this warpgroup's P columns of TMEM (the A
         // operand of the P V product): key 2c in the low half of column c
