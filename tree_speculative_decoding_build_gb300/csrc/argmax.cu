@@ -357,11 +357,22 @@ __global__ void argmax_stream_merge_kernel(const float *__restrict__ part_v,
     if (s0 == str_split(c + 1, nv, owners)) return -1;
     return 2 * c + ((c == c0 && s0 < rs) ? 1 : 0);
   };
-  const long long first = slot_of(c0 + lane);
+  // up to kArgHeld * 32 pieces (a few rows cut into many warp ranges) are
+  // worked out before the wait and then read all at once
+  constexpr int kArgHeld = 8;
+  long long held[kArgHeld];
+#pragma unroll
+  for (int h = 0; h < kArgHeld; ++h) held[h] = slot_of(c0 + lane + 32LL * h);
   pdl_wait();
+  Best got[kArgHeld];
+#pragma unroll
+  for (int h = 0; h < kArgHeld; ++h)
+    got[h] = held[h] >= 0 ? Best{part_v[held[h]], part_i[held[h]]} : Best{-INFINITY, INT32_MAX};
   Best me{-INFINITY, INT32_MAX};
-  if (first >= 0) merge(me, Best{part_v[first], part_i[first]});
-  for (long long c = c0 + lane + 32; c <= c1; c += 32) {  // rows cut into more than 32 pieces
+#pragma unroll
+  for (int h = 0; h < kArgHeld; ++h)
+    if (held[h] >= 0) merge(me, got[h]);
+  for (long long c = c0 + lane + 32LL * kArgHeld; c <= c1; c += 32) {  // rows cut into still more pieces
     const long long slot = slot_of(c);
     if (slot >= 0) merge(me, Best{part_v[slot], part_i[slot]});
   }
