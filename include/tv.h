@@ -30,10 +30,15 @@
  *     kernel before them is still running, but only when that kernel is one of
  *     this library's that releases its dependents early, and they read what
  *     that kernel writes only after it has completed.  tv_tree_attention reads
- *     q, the tree K/V, the KV cache and the block table early; none of this
- *     library's kernels that release their dependents early writes any of
- *     those (tv_commit_kv, which writes the cache, releases nothing early), and
- *     a caller's own kernel releases nothing early, so stream order applies.
+ *     q, the context lengths, the tree K/V, the KV cache and the block table
+ *     early; none of this library's kernels that release their dependents
+ *     early writes any of those (tv_commit_kv, which writes the cache and the
+ *     context lengths, releases nothing early), and a caller's own kernel
+ *     releases nothing early, so stream order applies.  tv_tree_attention's
+ *     own grids release their dependents early too, so its `out` must not be
+ *     the `q` of a tv_tree_attention call enqueued directly after it: a
+ *     caller's kernel between the two (as a model's projection is) restores
+ *     plain stream order.
  *   - The return value reports argument/shape validation and launch errors
  *     only.  Data errors found on the device (a malformed tree, a bad block id)
  *     are written to the per-sequence `status` array (int32 [B]): 0 = ok, else a

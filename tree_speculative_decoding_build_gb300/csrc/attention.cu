@@ -46,6 +46,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // hh = lane%2 of the head dimension (8-element groups interleaved by half), so
 // a warp computes 16 dot products per row with one shuffle to join halves.
 // In the P.V phase lane l owns output dims [l*D/32, (l+1)*D/32).
+// Launched as a programmatic dependent of the kernel before it: context
+// lengths and Q are read before griddepcontrol.wait; positions, ancestor
+// masks, block tables and every write come after it.
 template <int D>
 __global__ void __launch_bounds__(kCcThreads, D >= 256 ? 2 : 1)
 attn_generic_kernel(const AttnParams p) {
@@ -69,11 +72,17 @@ attn_generic_kernel(const AttnParams p) {
   const int r0 = blockIdx.z * kCcRows;
   const int nrows = min(kCcRows, p.R - r0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the combine grid launched after this one may be scheduled now: it waits
+  // for this grid's completion before reading the partials
+  pdl_launch_dependents();
 
   int ctx = p.ctx_len[b];
   const int ctx_cap = p.max_blocks * kBlock;
   if (ctx < 0 || ctx > ctx_cap) {
-    if (tid == 0) set_status(p.status, b, TV_ERR_BLOCK);
+    if (tid == 0) {
+      pdl_wait();
+      set_status(p.status, b, TV_ERR_BLOCK);
+    }
     ctx = ctx < 0 ? 0 : ctx_cap;
   }
   const int blk_lo = first_visible_block(ctx, p.window_left);
@@ -95,6 +104,10 @@ attn_generic_kernel(const AttnParams p) {
                            bf16_lo(w.y) * p.qscale, bf16_hi(w.y) * p.qscale);
     *reinterpret_cast<float4 *>(q_s + rr * D + c4 * 4) = f;
   }
+  // positions and ancestor masks come from the ancestor kernel before this
+  // grid, and every write below (status, partials, output) may race with the
+  // grid before: wait for its completion here
+  pdl_wait();
   for (int rr = tid; rr < nrows; rr += kCcThreads) {
     const int t = (r0 + rr) / p.G;
     if (!TV_CHECK(t < p.N && rr < kCcRows)) continue;
@@ -282,6 +295,9 @@ attn_generic_kernel(const AttnParams p) {
 
 // One warp per output row: O = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
 __global__ void attn_combine_kernel(const AttnParams p) {
+  // A grid launched after this one as a programmatic dependent reads, before
+  // its own wait, nothing this grid writes.
+  pdl_launch_dependents();
   // One warp per output row.  The split maxima and weights are formed by the
   // lanes in parallel (lane j holds split c*32 + j of each chunk of 32); the
   // weighted sum walks the splits four at a time so their loads overlap.
@@ -294,6 +310,7 @@ __global__ void attn_combine_kernel(const AttnParams p) {
   const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
   const int D = p.D;
   const size_t pr0 = (size_t)bk * p.splits * p.R + r;  // partial row of split s: pr0 + s * R
+  pdl_wait();  // the partials are the attention grid's output
   float M = -INFINITY;
   for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_ml[pr0 + (size_t)s * p.R].x);
 #pragma unroll
@@ -359,7 +376,7 @@ void launch_generic_d(const AttnParams &p, cudaStream_t stream) {
   cudaFuncSetAttribute(attn_generic_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   dim3 grid(p.B * p.Hkv, p.splits, (p.R + kCcRows - 1) / kCcRows);
-  attn_generic_kernel<D><<<grid, kCcThreads, smem, stream>>>(p);
+  launch_pdl(attn_generic_kernel<D>, grid, dim3(kCcThreads), smem, stream, p);
 }
 
 struct SplitPlan {
@@ -395,7 +412,7 @@ bool shape_ok(const tv_attn_args *a) {
 void launch_combine(const AttnParams &p, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.Hkv * p.R;
   const int wpb = 8;
-  attn_combine_kernel<<<(unsigned)((rows + wpb - 1) / wpb), wpb * 32, 0, stream>>>(p);
+  launch_pdl(attn_combine_kernel, dim3((unsigned)((rows + wpb - 1) / wpb)), dim3(wpb * 32), 0, stream, p);
 }
 
 void launch_attention_generic(const AttnParams &p, cudaStream_t stream) {

@@ -27,6 +27,11 @@
 // [256, 512).  Scores live in the base-2 domain (q scaled by
 // log2(e)/sqrt(D)), as in the other attention kernels.  Every wait is bounded
 // (2 s); on expiry status[b] = TV_ERR_CUDA and the CTA winds down.
+// Programmatic dependent launch: the grid may start while the kernel before
+// it on the stream finishes.  Before griddepcontrol.wait it reads only inputs
+// that no earlier kernel of a verify step writes (context lengths, block
+// tables, Q, K/V); positions and ancestor masks are read, and status words,
+// partials and the output written, only after it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -140,7 +145,10 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   int ctx = p.ctx_len[b];
   const int cap = p.max_blocks * kBlock;
   if (ctx < 0 || ctx > cap) {
-    if (tid == 0 && split == 0) set_status(p.status, b, TV_ERR_BLOCK);
+    if (tid == 0 && split == 0) {
+      pdl_wait();
+      set_status(p.status, b, TV_ERR_BLOCK);
+    }
     ctx = ctx < 0 ? 0 : cap;
   }
   const Range rg = range_of(p, ctx, split);
@@ -171,6 +179,9 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
   const uint32_t tmem = s_tmem;
   volatile int *abort_flag = &s_abort;
   bool ok = true;
+  // the combine grid launched after this one may be scheduled now: it waits
+  // for this grid's completion before reading the partials
+  if (tid == 0) pdl_launch_dependents();
 
   if (warp == 0) {
     // ============================================================ producer
@@ -202,7 +213,10 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
           int id = (r > 0 && TV_CHECK(b < p.B && slot >= 0 && slot < p.max_blocks))
                        ? __ldg(p.block_table + (size_t)b * p.max_blocks + slot) : -1;
           if (r > 0 && (id < 0 || id >= p.num_blocks)) {
-            if (lane == 0) set_status(p.status, b, TV_ERR_BLOCK);
+            if (lane == 0) {
+              pdl_wait();
+              set_status(p.status, b, TV_ERR_BLOCK);
+            }
             r = 0;
           }
           ids[i] = id;
@@ -278,6 +292,7 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       int dummy = 0;  // copies still in flight get a bounded chance to land
       for (int k = j > kStages ? j - kStages : 0; k < j; ++k)
         wait_slow(smem_u32(&bars.kv_full[k % kStages]), (uint32_t)((k / kStages) & 1), &dummy);
+      pdl_wait();
       set_status(p.status, b, TV_ERR_CUDA);
     }
   } else if (warp == 1) {
@@ -347,7 +362,10 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     int dummy = 0;
     if (lane == 0) wait_slow(smem_u32(&bars.fin), 0, &dummy);
     __syncwarp();
-    if (!ok && lane == 0) set_status(p.status, b, TV_ERR_CUDA);
+    if (!ok && lane == 0) {
+      pdl_wait();
+      set_status(p.status, b, TV_ERR_CUDA);
+    }
   } else {
     // ============================================================ softmax
     const int quad = warp & 3;
@@ -358,18 +376,6 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     const int g = row_ok ? m - t * G : 0;
     const float qscale = p.qscale;
     const int wl = p.window_left;
-    int pos_t = 0;
-    unsigned long long allowed = 0;
-    if (row_ok && TV_CHECK(b < p.B && t < N)) {
-      pos_t = p.pos[(size_t)b * N + t];
-      allowed = p.anc[(size_t)b * N + t];
-      if (wl >= 0) {
-        unsigned long long win = 0;
-        for (int a = 0; a < N; ++a)
-          if (p.pos[(size_t)b * N + a] >= pos_t - wl) win |= 1ull << a;
-        allowed &= win;
-      }
-    }
     float m_used = -INFINITY, l = 0.f;
     if (rg.n_tiles > 0) {
       // Q row into TMEM (rows past R are zero)
@@ -391,6 +397,22 @@ attn_tc256_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.q_full));
+    }
+    // positions and ancestor masks come from the ancestor kernel before this
+    // grid, and every write below (status, partials, output) may race with
+    // the grid before: wait for its completion here
+    pdl_wait();
+    int pos_t = 0;
+    unsigned long long allowed = 0;
+    if (row_ok && TV_CHECK(b < p.B && t < N)) {
+      pos_t = p.pos[(size_t)b * N + t];
+      allowed = p.anc[(size_t)b * N + t];
+      if (wl >= 0) {
+        unsigned long long win = 0;
+        for (int a = 0; a < N; ++a)
+          if (p.pos[(size_t)b * N + a] >= pos_t - wl) win |= 1ull << a;
+        allowed &= win;
+      }
     }
     for (int j = 0; j < rg.n_tiles; ++j) {
       if (!(ok = warp_wait(smem_u32(&bars.s_full), (uint32_t)(j & 1), abort_flag))) break;
@@ -606,7 +628,8 @@ cudaError_t launch_attention_tc256(const AttnParams &p, cudaStream_t stream) {
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.B * p.Hkv, p.splits);
-  attn_tc256_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mk, mkr, mv, mvr, mtk, mtv, p);
+  e = launch_pdl(attn_tc256_kernel, grid, dim3(kThreads), kSmemBytes, stream, mk, mkr, mv, mvr, mtk, mtv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
