@@ -318,9 +318,12 @@ SMALL = [
 ]
 
 # (kernel, num_splits): automatic choice (tensor cores for head dims 128 and
-# 256), then the CUDA-core kernel with one and with three context splits, and
-# the tensor cores asked for explicitly (with three splits at head dim 256)
-MODES = [(0, 0), (1, 1), (1, 3), (2, 0), (2, 3)]
+# 256), then the CUDA-core kernel with one, three and twenty context splits
+# (the split combine loads up to 16 splits' partials in one round and walks
+# more in batches: twenty takes the second path wherever the context has
+# twenty blocks), and the tensor cores asked for explicitly (with three splits
+# at head dim 256)
+MODES = [(0, 0), (1, 1), (1, 3), (1, 20), (2, 0), (2, 3)]
 
 
 @pytest.mark.parametrize("case", range(len(SMALL)))

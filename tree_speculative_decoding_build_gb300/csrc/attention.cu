@@ -294,14 +294,17 @@ attn_generic_kernel(const AttnParams p) {
 }
 
 // One warp per output row: O = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+constexpr int kCombAtOnce = 16;  // splits whose partials are loaded in one round
 __global__ void attn_combine_kernel(const AttnParams p) {
   // A grid launched after this one as a programmatic dependent reads, before
   // its own wait, nothing this grid writes.
   pdl_launch_dependents();
-  // One warp per output row.  The split maxima and weights are formed by the
-  // lanes in parallel (lane j holds split c*32 + j of each chunk of 32); the
-  // weighted sum walks the splits four at a time so their loads overlap.
-  // Lane l owns dims 8l .. 8l+7 (D <= 256).
+  // One warp per output row; lane l owns dims 8l .. 8l+7 (D <= 256).  With at
+  // most kCombAtOnce splits every partial is loaded in one round.  Otherwise
+  // the split maxima and weights are formed by the lanes in parallel (lane j
+  // holds split c*32 + j of each chunk of 32) and the weighted sum walks the
+  // splits four at a time so their loads overlap.  Both merge the splits in
+  // increasing order, so they give the same bits.
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)p.B * p.Hkv * p.R;
@@ -311,46 +314,81 @@ __global__ void attn_combine_kernel(const AttnParams p) {
   const int D = p.D;
   const size_t pr0 = (size_t)bk * p.splits * p.R + r;  // partial row of split s: pr0 + s * R
   pdl_wait();  // the partials are the attention grid's output
-  float M = -INFINITY;
-  for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_ml[pr0 + (size_t)s * p.R].x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float L = 0.f;
   float acc[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) acc[e] = 0.f;
   const bool mine = lane * 8 < D;
-  for (int c0 = 0; c0 < p.splits; c0 += 32) {
-    // this chunk's weights, one split per lane
-    const int sl = c0 + lane;
-    float wl = 0.f;
-    if (sl < p.splits) {
-      const float2 ml = p.part_ml[pr0 + (size_t)sl * p.R];
-      if (ml.x != -INFINITY) {
-        wl = exp2f(ml.x - M);
-        L += ml.y * wl;
+  if (p.splits <= kCombAtOnce) {
+    // Up to kCombAtOnce splits: every split's (max, sum) and O slice are
+    // loaded in one round, then merged in split order as below.  The O of a
+    // split with weight 0 (no keys) is loaded but not used.
+    const int n = p.splits;
+    const float2 ml = lane < n ? p.part_ml[pr0 + (size_t)lane * p.R] : make_float2(-INFINITY, 0.f);
+    float4 va[kCombAtOnce], vb[kCombAtOnce];
+#pragma unroll
+    for (int u = 0; u < kCombAtOnce; ++u) {
+      if (u < n && mine) {
+        const float *src = p.part_o + (pr0 + (size_t)u * p.R) * D + lane * 8;
+        va[u] = *reinterpret_cast<const float4 *>(src);
+        vb[u] = *reinterpret_cast<const float4 *>(src + 4);
       }
     }
-    const int n = min(32, p.splits - c0);
-    for (int j = 0; j < n; j += 4) {
-      float4 va[4], vb[4];
-      float w[4];
+    float M = ml.x;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        w[u] = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
-        if (j + u < n && w[u] != 0.f && mine) {
-          const float *src = p.part_o + (pr0 + (size_t)(c0 + j + u) * p.R) * D + lane * 8;
-          va[u] = *reinterpret_cast<const float4 *>(src);
-          vb[u] = *reinterpret_cast<const float4 *>(src + 4);
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float wl = 0.f;
+    if (ml.x != -INFINITY) {
+      wl = exp2f(ml.x - M);
+      L += ml.y * wl;
+    }
+#pragma unroll
+    for (int u = 0; u < kCombAtOnce; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wl, u);
+      if (u < n && w != 0.f && mine) {
+        acc[0] += va[u].x * w; acc[1] += va[u].y * w;
+        acc[2] += va[u].z * w; acc[3] += va[u].w * w;
+        acc[4] += vb[u].x * w; acc[5] += vb[u].y * w;
+        acc[6] += vb[u].z * w; acc[7] += vb[u].w * w;
+      }
+    }
+  } else {
+    float M = -INFINITY;
+    for (int s = lane; s < p.splits; s += 32) M = fmaxf(M, p.part_ml[pr0 + (size_t)s * p.R].x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    for (int c0 = 0; c0 < p.splits; c0 += 32) {
+      // this chunk's weights, one split per lane
+      const int sl = c0 + lane;
+      float wl = 0.f;
+      if (sl < p.splits) {
+        const float2 ml = p.part_ml[pr0 + (size_t)sl * p.R];
+        if (ml.x != -INFINITY) {
+          wl = exp2f(ml.x - M);
+          L += ml.y * wl;
         }
       }
+      const int n = min(32, p.splits - c0);
+      for (int j = 0; j < n; j += 4) {
+        float4 va[4], vb[4];
+        float w[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (j + u < n && w[u] != 0.f && mine) {
-          acc[0] += va[u].x * w[u]; acc[1] += va[u].y * w[u];
-          acc[2] += va[u].z * w[u]; acc[3] += va[u].w * w[u];
-          acc[4] += vb[u].x * w[u]; acc[5] += vb[u].y * w[u];
-          acc[6] += vb[u].z * w[u]; acc[7] += vb[u].w * w[u];
+        for (int u = 0; u < 4; ++u) {
+          w[u] = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
+          if (j + u < n && w[u] != 0.f && mine) {
+            const float *src = p.part_o + (pr0 + (size_t)(c0 + j + u) * p.R) * D + lane * 8;
+            va[u] = *reinterpret_cast<const float4 *>(src);
+            vb[u] = *reinterpret_cast<const float4 *>(src + 4);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          if (j + u < n && w[u] != 0.f && mine) {
+            acc[0] += va[u].x * w[u]; acc[1] += va[u].y * w[u];
+            acc[2] += va[u].z * w[u]; acc[3] += va[u].w * w[u];
+            acc[4] += vb[u].x * w[u]; acc[5] += vb[u].y * w[u];
+            acc[6] += vb[u].z * w[u]; acc[7] += vb[u].w * w[u];
+          }
         }
       }
     }
@@ -411,7 +449,10 @@ bool shape_ok(const tv_attn_args *a) {
 
 void launch_combine(const AttnParams &p, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.Hkv * p.R;
-  const int wpb = 8;
+  // 4 warps (128 threads) per block: a block holds the partials of up to 16
+  // splits in registers (about 21K), which leaves room on its SM for a CTA of
+  // the attention launched after it, as a programmatic dependent, to start
+  const int wpb = 4;
   launch_pdl(attn_combine_kernel, dim3((unsigned)((rows + wpb - 1) / wpb)), dim3(wpb * 32), 0, stream, p);
 }
 
