@@ -319,6 +319,7 @@ topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chun
     const int w0 = (int)((long long)nvec * w / kTopWarps);
     const int w1 = (int)((long long)nvec * (w + 1) / kTopWarps);
     const uint4 *xv = reinterpret_cast<const uint4 *>(xr + begin);
+    bool fresh = true;  // the list does not hold k entries yet
     for (int b0 = w0; b0 < w1; b0 += 32 * kTopUnroll) {
       uint4 q[kTopUnroll];
 #pragma unroll
@@ -327,13 +328,51 @@ topk_chunk_kernel(const T *__restrict__ x, int V, long long row_stride, int chun
         if (j < w1) q[u] = __ldcs(xv + j);
       }
       const float bar = fkey_inv(*(volatile int *)&s_bar);
+      if (fresh) {
+        // A list short of k entries would take nearly every element as an
+        // insert of its own.  Each lane's best element of the batch goes in by
+        // one fold instead (32 candidates at once), as in the streaming plan;
+        // the lanes' other elements then go through take_own, which skips the
+        // one already in (excl).  A vector whose maximum ties the k-th entry
+        // may still hold a lower index that beats it, so ties are examined too.
+        float lm = -INFINITY;
+        int im = INT32_MAX;
 #pragma unroll
-      for (int u = 0; u < kTopUnroll; ++u) {
-        const int j = b0 + lane + 32 * u;
-        const float m = vec_max<T>(q[u]);
-        const bool flag = j < w1 && (m > tv || ti == INT32_MAX) && !(m < bar);
-        const unsigned ballot = __ballot_sync(0xffffffffu, flag);
-        if (ballot) take_flagged<T>(ballot, q[u], begin + j * E, k, lv, li, tv, ti);
+        for (int u = 0; u < kTopUnroll; ++u) {
+          const int j = b0 + lane + 32 * u;
+          if (j < w1) {
+            const float m = vec_max<T>(q[u]);
+            if (m > lm) {  // the earliest vector holding the lane's maximum
+              int e = E - 1;
+#pragma unroll
+              for (int ee = E - 1; ee >= 0; --ee)
+                if (vec_elem<T>(q[u], ee) == m) e = ee;
+              lm = m;
+              im = begin + j * E + e;
+            }
+          }
+        }
+        fold32(lv, li, lm, im);
+        tv = __shfl_sync(0xffffffffu, lv, k - 1);
+        ti = __shfl_sync(0xffffffffu, li, k - 1);
+#pragma unroll
+        for (int u = 0; u < kTopUnroll; ++u) {
+          const int j = b0 + lane + 32 * u;
+          const float m = vec_max<T>(q[u]);
+          const bool flag = j < w1 && (m >= tv || ti == INT32_MAX) && !(m < bar);
+          const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+          if (ballot) take_own<T>(flag, q[u], begin + j * E, im, k, lv, li, tv, ti);
+        }
+        fresh = ti == INT32_MAX;
+      } else {
+#pragma unroll
+        for (int u = 0; u < kTopUnroll; ++u) {
+          const int j = b0 + lane + 32 * u;
+          const float m = vec_max<T>(q[u]);
+          const bool flag = j < w1 && (m > tv || ti == INT32_MAX) && !(m < bar);
+          const unsigned ballot = __ballot_sync(0xffffffffu, flag);
+          if (ballot) take_flagged<T>(ballot, q[u], begin + j * E, k, lv, li, tv, ti);
+        }
       }
       if (lane == 0 && ti != INT32_MAX) atomicMax(&s_bar, fkey(tv));
     }
