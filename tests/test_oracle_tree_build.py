@@ -185,8 +185,8 @@ def test_hand_examples():
     t1 = tb.build_tree_one(vals, toks, 3, w=1)
     assert list(t1["tokens"]) == [10, 20, 21] and list(t1["parent"]) == [-1, 0, 0]
     assert list(t1["score"]) == [np.float32(-1.0), np.float32(-1.5), np.float32(-1.6)]
-    # w = 2: round 1 pops both roots (the only candidates); round 2 takes the one
-    # remaining slot, child 20 of root 10 (-1.5).
+    # w = 2: the first expansion round pops both roots (the only candidates); the
+    # second takes the one remaining slot, child 20 of root 10 (-1.5).
     t2 = tb.build_tree_one(vals, toks, 3, w=2)
     assert list(t2["tokens"]) == [10, 11, 20] and list(t2["parent"]) == [-1, -1, 0]
     assert t2["rounds"] == 2
