@@ -73,3 +73,29 @@ def test_every_step_sees_its_whole_upload(fake_cuda, steps):
     assert len(seen) == 2 + steps                   # two warm-up steps, then the timed ones
     assert seen[2:] == [s % 2 for s in range(steps)]
     assert res[0].item() == len(seen)               # the last step's results were read back
+
+
+def test_passes_report_the_median_and_time_only_the_passes(monkeypatch):
+    # stand-in events whose timed intervals are 9, 3 and 6 ms: the median is 6
+    lengths = iter([9.0, 3.0, 6.0])
+
+    class _TimedEvent(_Event):
+        def elapsed_time(self, other):
+            return next(lengths)
+
+    monkeypatch.setattr(torch.cuda, "Stream", _Stream)
+    monkeypatch.setattr(torch.cuda, "Event", _TimedEvent)
+    monkeypatch.setattr(torch.cuda, "stream", lambda s: contextlib.nullcontext())
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda device=None: None)
+    host = {"tokens": torch.arange(5, dtype=torch.int32)}
+    bufs = [{k: torch.zeros_like(v) for k, v in host.items()} for _ in range(2)]
+    calls = []
+
+    def step(d):
+        assert torch.equal(d["tokens"], host["tokens"])
+        calls.append(1)
+
+    steps = 3
+    ms = bench.pipelined_e2e(step, host, bufs, [], steps, _Stream(), "cpu", passes=3)
+    assert ms == pytest.approx(6.0 / steps)
+    assert len(calls) == 2 + 3 * steps            # one warm-up, then every pass
